@@ -1,0 +1,201 @@
+/*
+ * mla_b300.h -- C ABI of the B300 (sm_103a) absorbed, paged MLA decode path.
+ *
+ * What the path computes (Multi-head Latent Attention, DeepSeek-V2):
+ *   "DeepSeek-V2: Multi-Head Latent Attention (MLA) 原理与工程实现"
+ *   (PaperTrace) -- 2.1 joint KV down-projection and up-projection,
+ *   2.2 matrix absorption at inference, 2.3 query compression,
+ *   3.2 decoupled RoPE (score = content part in the latent space + position
+ *   part), 3.3 the cached row c_KV | k_R.
+ *   "DeepSeek R1的MLA：KV缓存的低秩压缩革命" -- 二 2.2 (precomputing
+ *   Q W_uk^T), 五 item 4 (paged KV cache).
+ *
+ * One decode step, as the calls run on one stream:
+ *   mla_append_latent  x W^DKV|W^KR, RoPE on k_R, store into the paged cache
+ *   mla_project_q      [W^UQ|W^QR] (W^DQ x), RoPE on q_R
+ *   mla_absorb_q       q_cat = [W^UK_h^T q_C,h | q_R,h]       (per head)
+ *   mla_plan_decode    balanced split of all sequences' pages over the SMs
+ *   mla_decode_attn    scores q_cat . [c | k_R], online softmax, latent output
+ *   mla_combine        log-sum-exp merge of the split partial results
+ *   mla_absorb_out     o_h = W^UV_h o_lat,h                    (per head)
+ *   mla_out_proj       u = W^O [o_1; ...; o_n_h]
+ *
+ * Conventions that hold for every call:
+ *   - Every pointer argument except `dims` is DEVICE memory owned by the
+ *     caller; the library never allocates, frees or keeps a pointer past the
+ *     call. `dims` is host memory, read during the call only.
+ *   - Every call only enqueues work on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream) and returns without waiting.
+ *   - Weights use the column-vector convention W in R^{out x in}, stored
+ *     row-major [out][in]; per-head blocks are consecutive rows.
+ *   - Tensors are dense and row-major in the shapes given; element type is
+ *     `dtype` (MLA_F32 = float, MLA_BF16 = bfloat16 bits) unless the
+ *     signature says float.
+ *   - Return value: MLA_OK, or an error found on the host before anything is
+ *     enqueued (MLA_ERR_INVALID_ARG / UNSUPPORTED / WORKSPACE), or
+ *     MLA_ERR_CUDA if a launch failed. mla_last_error() gives a message.
+ *   - Errors found on the device (a block id outside the page pool, a
+ *     position or length past the block table) cannot be returned: kernels
+ *     OR a bit (MLA_DEV_*) into the caller's int32 `dev_status` word, skip
+ *     the offending access, and carry on. Read the word after the stream
+ *     has synchronised; `dev_status` may be NULL to skip the checks' report
+ *     (the accesses are still skipped).
+ */
+#ifndef MLA_B300_H
+#define MLA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_ABI_VERSION 1
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size   */
+  MLA_ERR_UNSUPPORTED = 2, /* shape/dtype this build has no kernel for      */
+  MLA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
+  MLA_ERR_CUDA = 4         /* a CUDA launch or query failed                 */
+} mla_status;
+
+/* Bits kernels OR into *dev_status. */
+#define MLA_DEV_BAD_BLOCK 0x1   /* block-table entry outside [0, num_pages)  */
+#define MLA_DEV_BAD_POS 0x2     /* position outside the block table / RoPE   */
+#define MLA_DEV_BAD_LEN 0x4     /* sequence length < 1 or past the table     */
+#define MLA_DEV_TIMEOUT 0x8     /* a bounded wait inside a kernel gave up    */
+
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/* Model dimensions (notation of the DeepSeek-V2 MLA page, 1.1 / 2.1 / 3.2). */
+typedef struct {
+  int n_h;       /* attention heads                                   */
+  int d_h;       /* per-head no-PE query/key width                    */
+  int d_r;       /* decoupled RoPE width d_h^R (even)                 */
+  int d_c;       /* KV latent width                                   */
+  int d_v;       /* per-head value width                              */
+  int d_model;   /* hidden size d (append / project_q / out_proj)     */
+  int d_cq;      /* query latent width d_c'; 0 = no query compression */
+  int page_size; /* tokens per cache page                             */
+} mla_dims;
+
+/* Name of a status code; never NULL. */
+const char* mla_status_string(int status);
+/* Detail of the last non-OK status returned on this host thread. */
+const char* mla_last_error(void);
+int mla_abi_version(void);
+
+/* RoPE table (RoFormer, which the MLA page's lineage section cites):
+ * cos_sin[p][i] = {cos(p*theta_i), sin(p*theta_i)}, theta_i =
+ * base^(-2i/d_r), for p < max_pos, i < d_r/2; computed in double, stored as
+ * float [max_pos][d_r/2][2]. */
+mla_status mla_rope_table(float* cos_sin, int max_pos, int d_r, double base, void* stream);
+
+/* (a1) Append latent rows -- DeepSeek-V2 MLA page 2.1 (c_KV = W^DKV h) and
+ * 3.2 (k_R = RoPE(W^KR h), cached beside c_KV, not compressed).
+ *   x          [T][d_model]                 token hidden states
+ *   w_dkv_kr   [d_c + d_r][d_model]         rows of W^DKV, then of W^KR
+ *   seq_idx    [T] int32 or NULL            sequence of token t (NULL: t)
+ *   pos        [T] int32                    position of token t
+ *   block_table[B][max_pages] int32         physical page of each logical page
+ *   rope       [max_pos][d_r/2][2] float    from mla_rope_table
+ *   cache      [num_pages][page_size][d_c + d_r]   written at row
+ *              (block_table[s][pos/page_size], pos%page_size); nothing else.
+ * fp32 accumulation; the row is rounded once to `dtype` on store.
+ * Device checks: seq_idx in [0,B), pos in [0, max_pages*page_size) and
+ * < max_pos, block id in [0, num_pages). */
+mla_status mla_append_latent(const void* x, const void* w_dkv_kr, const int32_t* seq_idx,
+                             const int32_t* pos, const int32_t* block_table, int B,
+                             int max_pages, int num_pages, int T, const float* rope,
+                             int max_pos, void* cache, mla_dtype dtype, const mla_dims* dims,
+                             int32_t* dev_status, void* stream);
+
+/* (a2) Query projection -- DeepSeek-V2 MLA page 2.3 (c_Q = W^DQ h,
+ * q_C = W^UQ c_Q) and 3.2 (q_R = RoPE(W^QR c_Q), one slice per head).
+ *   x        [T][d_model]
+ *   w_dq     [d_cq][d_model], or NULL when dims->d_cq == 0 (then c_Q = x)
+ *   w_uq_qr  [n_h][d_h + d_r][K], K = d_cq or d_model: per head the rows of
+ *            W^UQ_h then of W^QR_h
+ *   pos      [T] int32, rope as for mla_append_latent
+ *   c_q      [T][d_cq] scratch the caller provides (ignored if d_cq == 0)
+ *   q        [T][n_h][d_h + d_r] output: [q_C,h | RoPE(q_R,h)]
+ * fp32 accumulation; c_q and q are stored in `dtype`. */
+mla_status mla_project_q(const void* x, const void* w_dq, const void* w_uq_qr,
+                         const int32_t* pos, int T, const float* rope, int max_pos,
+                         void* c_q, void* q, mla_dtype dtype, const mla_dims* dims,
+                         int32_t* dev_status, void* stream);
+
+/* (a3) Absorb W^UK into the query -- DeepSeek-V2 MLA page 2.2
+ * (q^T W^UK c = (W^UK^T q)^T c); R1 MLA page 二 2.2 (precompute Q W_uk^T).
+ *   q      [B][n_h][d_h + d_r]
+ *   w_uk   [n_h*d_h][d_c]           (W^UK, head h = rows h*d_h ..)
+ *   q_cat  [B][n_h][d_c + d_r]      output: [W^UK_h^T q_C,h | q_R,h]
+ * fp32 accumulation, one rounding to `dtype`. */
+mla_status mla_absorb_q(const void* q, const void* w_uk, void* q_cat, int B, mla_dtype dtype,
+                        const mla_dims* dims, void* stream);
+
+/* (a4) Split plan. The pages of all sequences, in order, are cut into
+ * contiguous ranges of near-equal cost, one per worker (an SM or SM pair of
+ * the decode kernel the same dtype/dims select); a sequence cut into k > 1
+ * ranges gets k partial results that mla_combine merges. The plan lives in
+ * `workspace` and depends only on seq_lens, B, dtype, dims and the device.
+ *   seq_lens [B] int32 (>= 1; tokens already in the cache, including the
+ *            one being decoded). */
+size_t mla_decode_workspace_size(int B, mla_dtype dtype, const mla_dims* dims);
+mla_status mla_plan_decode(const int32_t* seq_lens, int B, int max_pages, void* workspace,
+                           size_t ws_bytes, mla_dtype dtype, const mla_dims* dims,
+                           int32_t* dev_status, void* stream);
+
+/* (a5) Paged split-KV decode attention in the latent space -- DeepSeek-V2
+ * MLA page 3.2: s_j = (q_abs . c_j + q_R . k_R,j) * softmax_scale over the
+ * sequence's cached tokens j < seq_lens[b]; softmax; o_lat = sum_j p_j c_j.
+ *   q_cat   [B][n_h][d_c + d_r]        from mla_absorb_q
+ *   cache   [num_pages][page_size][d_c + d_r]
+ *   block_table [B][max_pages] int32, seq_lens [B] int32
+ *   workspace   planned by mla_plan_decode with the same seq_lens
+ *   o_lat   [B][n_h][d_c] float, lse [B][n_h] float (natural log of
+ *           sum_j exp(s_j)): written for sequences the plan does not split;
+ *           split sequences are written by mla_combine.
+ * bf16 path: bf16 tensor-core products with fp32 accumulation; probabilities
+ * are rounded to bf16 before the P.V product. f32 path: fp32 throughout. */
+mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* block_table,
+                           int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                           float softmax_scale, void* workspace, size_t ws_bytes, float* o_lat,
+                           float* lse, mla_dtype dtype, const mla_dims* dims,
+                           int32_t* dev_status, void* stream);
+
+/* (a6) Merge split partials: lse = log sum_s exp(lse_s),
+ * o_lat = sum_s exp(lse_s - lse) o_s, for every sequence the plan split. */
+mla_status mla_combine(const void* workspace, size_t ws_bytes, int B, float* o_lat, float* lse,
+                       mla_dtype dtype, const mla_dims* dims, void* stream);
+
+/* (a7) Map the latent output back per head -- DeepSeek-V2 MLA page 2.2
+ * (the W^UV half of W~^O = W^O W^UV, applied unfused).
+ *   o_lat [B][n_h][d_c] float; w_uv [n_h*d_v][d_c] in `dtype`;
+ *   o     [B][n_h*d_v] in `out_dtype`. fp32 accumulation. */
+mla_status mla_absorb_out(const float* o_lat, const void* w_uv, void* o, int B, mla_dtype dtype,
+                          mla_dtype out_dtype, const mla_dims* dims, void* stream);
+
+/* (a8) Output projection u = W^O [o_1; ...; o_n_h] -- DeepSeek-V2 MLA
+ * page 2.2 (W^O).
+ *   o [B][n_h*d_v] in `dtype`; w_o [d_model][n_h*d_v] in `dtype`;
+ *   u [B][d_model] float. fp32 accumulation. */
+mla_status mla_out_proj(const void* o, const void* w_o, float* u, int B, mla_dtype dtype,
+                        const mla_dims* dims, void* stream);
+
+/* Which decode kernel the given dtype/dims select on the current device:
+ * 1 = tcgen05 tensor-core kernel, 0 = CUDA-core (SIMT) kernel. */
+int mla_decode_path(mla_dtype dtype, const mla_dims* dims);
+
+/* Pin the decode kernel choice for this process: 0 = always the SIMT kernel,
+ * 1 = the tcgen05 kernel wherever it supports the shape, -1 = automatic
+ * (default). Plans, workspaces and decode calls must be made under the same
+ * setting. Used to cross-check the two kernels against each other. */
+void mla_force_decode_path(int path);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_B300_H */

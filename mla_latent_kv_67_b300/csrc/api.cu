@@ -1,0 +1,310 @@
+// C ABI entry points: argument checks on the host, then kernel dispatch.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_decode.h"
+
+using namespace mla;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mla_status fail(mla_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = std::string(mla_status_string(st)) + ": " + buf;
+  return st;
+}
+
+mla_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MLA_OK;
+  return fail(MLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define REQUIRE(cond, ...) \
+  do {                     \
+    if (!(cond)) return fail(MLA_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+mla_status check_dims(const mla_dims* d) {
+  REQUIRE(d != nullptr, "dims is NULL");
+  REQUIRE(d->n_h > 0 && d->d_h > 0 && d->d_c > 0 && d->d_v > 0 && d->page_size > 0,
+          "dims must be positive (n_h=%d d_h=%d d_c=%d d_v=%d page_size=%d)", d->n_h, d->d_h,
+          d->d_c, d->d_v, d->page_size);
+  REQUIRE(d->d_r >= 0 && d->d_r % 2 == 0, "d_r must be even and >= 0 (got %d)", d->d_r);
+  REQUIRE(d->d_model >= 0 && d->d_cq >= 0, "d_model and d_cq must be >= 0");
+  return MLA_OK;
+}
+
+mla_status check_dtype(int dt) {
+  REQUIRE(dt == MLA_F32 || dt == MLA_BF16, "unknown dtype %d", dt);
+  return MLA_OK;
+}
+
+int g_forced_path = -1;
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+int pick_path(mla_dtype dt, const mla_dims* d) {
+  if (g_forced_path == 0) return 0;
+  const bool tc_ok = dt == MLA_BF16 && tc_decode_supported(d->n_h, d->d_c, d->d_r, d->page_size);
+  if (g_forced_path == 1) return tc_ok ? 1 : 0;
+  return tc_ok ? 1 : 0;
+}
+
+int workers_for(int path) {
+  const int sms = device_sms();
+  if (sms <= 0) return 0;
+  return path == 1 ? tc_decode_workers(sms) : sms;
+}
+
+cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int st) {
+  switch (st) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+const char* mla_last_error(void) { return g_last_error.c_str(); }
+
+int mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+void mla_force_decode_path(int path) { g_forced_path = (path == 0 || path == 1) ? path : -1; }
+
+int mla_decode_path(mla_dtype dtype, const mla_dims* dims) {
+  if (check_dims(dims) != MLA_OK || check_dtype(dtype) != MLA_OK) return -1;
+  return pick_path(dtype, dims);
+}
+
+mla_status mla_rope_table(float* cos_sin, int max_pos, int d_r, double base, void* stream) {
+  REQUIRE(cos_sin != nullptr, "cos_sin is NULL");
+  REQUIRE(max_pos >= 0 && d_r > 0 && d_r % 2 == 0, "bad max_pos=%d / d_r=%d", max_pos, d_r);
+  REQUIRE(base > 0.0, "base must be > 0");
+  return cuda_status(launch_rope_table(cos_sin, max_pos, d_r, base, S(stream)), "rope_table");
+}
+
+mla_status mla_append_latent(const void* x, const void* w_dkv_kr, const int32_t* seq_idx,
+                             const int32_t* pos, const int32_t* block_table, int B,
+                             int max_pages, int num_pages, int T, const float* rope,
+                             int max_pos, void* cache, mla_dtype dtype, const mla_dims* dims,
+                             int32_t* dev_status, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(T >= 0 && B >= 0, "T and B must be >= 0");
+  if (T == 0) return MLA_OK;
+  REQUIRE(x && w_dkv_kr && pos && block_table && cache, "NULL tensor argument");
+  REQUIRE(dims->d_model > 0, "append needs d_model > 0");
+  REQUIRE(B > 0 && max_pages > 0 && num_pages > 0, "B, max_pages, num_pages must be > 0");
+  REQUIRE(dims->d_r == 0 || (rope && max_pos > 0), "RoPE table required when d_r > 0");
+  const int f32 = dtype == MLA_F32;
+  GemmArgs g = {};
+  g.a = x; g.a_gs = 0; g.a_ms = dims->d_model; g.a_f32 = f32;
+  g.w = w_dkv_kr; g.w_gs = 0; g.w_ns = dims->d_model; g.w_ks = 1; g.w_f32 = f32;
+  g.G = 1; g.M = T; g.N = dims->d_c + dims->d_r; g.K = dims->d_model;
+  g.epi = EPI_APPEND;
+  g.out = cache; g.o_f32 = f32;
+  g.rope = rope; g.max_pos = max_pos; g.d_r = dims->d_r; g.rope_off = dims->d_c;
+  g.rope_period = g.N; g.pos = pos;
+  g.seq_idx = seq_idx; g.block_table = block_table; g.B = B; g.max_pages = max_pages;
+  g.num_pages = num_pages; g.page_size = dims->page_size; g.dev_status = dev_status;
+  return cuda_status(launch_simt_gemm(g, S(stream)), "append_latent");
+}
+
+mla_status mla_project_q(const void* x, const void* w_dq, const void* w_uq_qr,
+                         const int32_t* pos, int T, const float* rope, int max_pos,
+                         void* c_q, void* q, mla_dtype dtype, const mla_dims* dims,
+                         int32_t* dev_status, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(T >= 0, "T must be >= 0");
+  if (T == 0) return MLA_OK;
+  REQUIRE(x && w_uq_qr && pos && q, "NULL tensor argument");
+  REQUIRE(dims->d_model > 0, "project_q needs d_model > 0");
+  REQUIRE(dims->d_cq == 0 || (w_dq && c_q), "d_cq > 0 needs w_dq and the c_q scratch");
+  REQUIRE(dims->d_r == 0 || (rope && max_pos > 0), "RoPE table required when d_r > 0");
+  const int f32 = dtype == MLA_F32;
+  const void* src = x;
+  int K = dims->d_model;
+  if (dims->d_cq > 0) {
+    GemmArgs g = {};
+    g.a = x; g.a_ms = dims->d_model; g.a_f32 = f32;
+    g.w = w_dq; g.w_ns = dims->d_model; g.w_ks = 1; g.w_f32 = f32;
+    g.G = 1; g.M = T; g.N = dims->d_cq; g.K = dims->d_model;
+    g.epi = EPI_STORE; g.out = c_q; g.o_ms = dims->d_cq; g.o_f32 = f32;
+    if ((st = cuda_status(launch_simt_gemm(g, S(stream)), "project_q/W^DQ")) != MLA_OK) return st;
+    src = c_q;
+    K = dims->d_cq;
+  }
+  const int per_head = dims->d_h + dims->d_r;
+  GemmArgs g = {};
+  g.a = src; g.a_ms = K; g.a_f32 = f32;
+  g.w = w_uq_qr; g.w_ns = K; g.w_ks = 1; g.w_f32 = f32;
+  g.G = 1; g.M = T; g.N = dims->n_h * per_head; g.K = K;
+  g.epi = EPI_ROPE; g.out = q; g.o_ms = g.N; g.o_f32 = f32;
+  g.rope = rope; g.max_pos = max_pos; g.d_r = dims->d_r; g.rope_off = dims->d_h;
+  g.rope_period = per_head; g.pos = pos; g.dev_status = dev_status;
+  return cuda_status(launch_simt_gemm(g, S(stream)), "project_q/W^UQ|W^QR");
+}
+
+mla_status mla_absorb_q(const void* q, const void* w_uk, void* q_cat, int B, mla_dtype dtype,
+                        const mla_dims* dims, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0, "B must be >= 0");
+  if (B == 0) return MLA_OK;
+  REQUIRE(q && w_uk && q_cat, "NULL tensor argument");
+  const int f32 = dtype == MLA_F32;
+  const int qw = dims->d_h + dims->d_r, cw = dims->d_c + dims->d_r;
+  GemmArgs g = {};
+  g.a = q; g.a_gs = qw; g.a_ms = (long long)dims->n_h * qw; g.a_f32 = f32;
+  g.w = w_uk; g.w_gs = (long long)dims->d_h * dims->d_c; g.w_ns = 1; g.w_ks = dims->d_c;
+  g.w_f32 = f32;
+  g.G = dims->n_h; g.M = B; g.N = dims->d_c; g.K = dims->d_h;
+  g.epi = EPI_STORE; g.out = q_cat; g.o_gs = cw; g.o_ms = (long long)dims->n_h * cw; g.o_f32 = f32;
+  if ((st = cuda_status(launch_simt_gemm(g, S(stream)), "absorb_q")) != MLA_OK) return st;
+  return cuda_status(launch_copy_rope_part(q, q_cat, B, dims->n_h, dims->d_h, dims->d_r,
+                                           dims->d_c, f32, S(stream)),
+                     "absorb_q/rope part");
+}
+
+size_t mla_decode_workspace_size(int B, mla_dtype dtype, const mla_dims* dims) {
+  if (check_dims(dims) != MLA_OK || check_dtype(dtype) != MLA_OK || B < 0) return 0;
+  const int workers = workers_for(pick_path(dtype, dims));
+  if (workers <= 0) return 0;
+  return workspace_layout(B, workers, dims->n_h, dims->d_c).total;
+}
+
+mla_status mla_plan_decode(const int32_t* seq_lens, int B, int max_pages, void* workspace,
+                           size_t ws_bytes, mla_dtype dtype, const mla_dims* dims,
+                           int32_t* dev_status, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0 && max_pages > 0, "B must be >= 0 and max_pages > 0");
+  if (B == 0) return MLA_OK;
+  REQUIRE(seq_lens != nullptr, "seq_lens is NULL");
+  const int path = pick_path(dtype, dims);
+  const int workers = workers_for(path);
+  if (workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
+  const WorkspaceLayout L = workspace_layout(B, workers, dims->n_h, dims->d_c);
+  if (!workspace || ws_bytes < L.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L.total);
+  return cuda_status(launch_plan(seq_lens, B, max_pages, dims->page_size, workers, path,
+                                 workspace, L, dev_status, S(stream)),
+                     "plan_decode");
+}
+
+mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* block_table,
+                           int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                           float softmax_scale, void* workspace, size_t ws_bytes, float* o_lat,
+                           float* lse, mla_dtype dtype, const mla_dims* dims,
+                           int32_t* dev_status, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0, "B must be >= 0");
+  if (B == 0) return MLA_OK;
+  REQUIRE(q_cat && cache && block_table && seq_lens && o_lat && lse, "NULL tensor argument");
+  REQUIRE(max_pages > 0 && num_pages > 0, "max_pages and num_pages must be > 0");
+  REQUIRE(dims->d_c % 32 == 0 && dims->d_c <= 512, "d_c must be a multiple of 32, <= 512");
+  const int path = pick_path(dtype, dims);
+  const int workers = workers_for(path);
+  if (workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
+  const WorkspaceLayout L = workspace_layout(B, workers, dims->n_h, dims->d_c);
+  if (!workspace || ws_bytes < L.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L.total);
+  (void)seq_lens;  // the plan in the workspace carries the validated lengths
+  if (path == 1)
+    return cuda_status(tc_decode_launch(q_cat, cache, block_table, max_pages, num_pages, B,
+                                        workers, softmax_scale, workspace, L, o_lat, lse,
+                                        dev_status, S(stream)),
+                       "decode_attn (tcgen05)");
+  return cuda_status(launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, B,
+                                        workers, softmax_scale, workspace, L, o_lat, lse,
+                                        dims->n_h, dims->d_c, dims->d_r, dims->page_size,
+                                        dtype == MLA_F32, dev_status, S(stream)),
+                     "decode_attn (simt)");
+}
+
+mla_status mla_combine(const void* workspace, size_t ws_bytes, int B, float* o_lat, float* lse,
+                       mla_dtype dtype, const mla_dims* dims, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0, "B must be >= 0");
+  if (B == 0) return MLA_OK;
+  REQUIRE(o_lat && lse, "NULL tensor argument");
+  const int workers = workers_for(pick_path(dtype, dims));
+  if (workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
+  const WorkspaceLayout L = workspace_layout(B, workers, dims->n_h, dims->d_c);
+  if (!workspace || ws_bytes < L.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L.total);
+  return cuda_status(launch_combine(workspace, L, B, dims->n_h, dims->d_c, o_lat, lse, S(stream)),
+                     "combine");
+}
+
+mla_status mla_absorb_out(const float* o_lat, const void* w_uv, void* o, int B, mla_dtype dtype,
+                          mla_dtype out_dtype, const mla_dims* dims, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  if ((st = check_dtype(out_dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0, "B must be >= 0");
+  if (B == 0) return MLA_OK;
+  REQUIRE(o_lat && w_uv && o, "NULL tensor argument");
+  GemmArgs g = {};
+  g.a = o_lat; g.a_gs = dims->d_c; g.a_ms = (long long)dims->n_h * dims->d_c; g.a_f32 = 1;
+  g.w = w_uv; g.w_gs = (long long)dims->d_v * dims->d_c; g.w_ns = dims->d_c; g.w_ks = 1;
+  g.w_f32 = dtype == MLA_F32;
+  g.G = dims->n_h; g.M = B; g.N = dims->d_v; g.K = dims->d_c;
+  g.epi = EPI_STORE; g.out = o; g.o_gs = dims->d_v; g.o_ms = (long long)dims->n_h * dims->d_v;
+  g.o_f32 = out_dtype == MLA_F32;
+  return cuda_status(launch_simt_gemm(g, S(stream)), "absorb_out");
+}
+
+mla_status mla_out_proj(const void* o, const void* w_o, float* u, int B, mla_dtype dtype,
+                        const mla_dims* dims, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0, "B must be >= 0");
+  if (B == 0) return MLA_OK;
+  REQUIRE(o && w_o && u, "NULL tensor argument");
+  REQUIRE(dims->d_model > 0, "out_proj needs d_model > 0");
+  const int K = dims->n_h * dims->d_v;
+  GemmArgs g = {};
+  g.a = o; g.a_ms = K; g.a_f32 = dtype == MLA_F32;
+  g.w = w_o; g.w_ns = K; g.w_ks = 1; g.w_f32 = dtype == MLA_F32;
+  g.G = 1; g.M = B; g.N = dims->d_model; g.K = K;
+  g.epi = EPI_STORE; g.out = u; g.o_ms = dims->d_model; g.o_f32 = 1;
+  return cuda_status(launch_simt_gemm(g, S(stream)), "out_proj");
+}
+
+}  // extern "C"

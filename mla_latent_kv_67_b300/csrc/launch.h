@@ -1,0 +1,52 @@
+// Host-side launchers shared between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace mla {
+
+// Generic CUDA-core batched GEMM with fused epilogues:
+//   out[g][m][n] = sum_k A[g][m][k] * W[g](n, k)
+// A element (g,m,k) at a + g*a_gs + m*a_ms + k;
+// W element (g,n,k) at w + g*w_gs + n*w_ns + k*w_ks.
+enum Epilogue {
+  EPI_STORE = 0,   // out + g*o_gs + m*o_ms + n
+  EPI_ROPE = 1,    // as STORE, RoPE on columns n%(rope_off+d_r) >= rope_off
+  EPI_APPEND = 2,  // RoPE on n >= rope_off, then scatter into the paged cache
+};
+
+struct GemmArgs {
+  const void* a; long long a_gs, a_ms; int a_f32;
+  const void* w; long long w_gs, w_ns, w_ks; int w_f32;
+  int G, M, N, K;
+  int epi;
+  void* out; long long o_gs, o_ms; int o_f32;
+  // RoPE (EPI_ROPE / EPI_APPEND)
+  const float* rope; int max_pos; int d_r; int rope_off; int rope_period;
+  const int32_t* pos;
+  // paged store (EPI_APPEND)
+  const int32_t* seq_idx; const int32_t* block_table; int B, max_pages, num_pages, page_size;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_simt_gemm(const GemmArgs& g, cudaStream_t s);
+cudaError_t launch_copy_rope_part(const void* q, void* q_cat, int B, int n_h, int d_h, int d_r,
+                                  int d_c, int f32, cudaStream_t s);
+cudaError_t launch_rope_table(float* cs, int max_pos, int d_r, double base, cudaStream_t s);
+
+cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32_t* block_table,
+                               int max_pages, int num_pages, int B, int workers, float scale,
+                               const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
+                               int n_h, int d_c, int d_r, int page_size, int f32,
+                               int32_t* dev_status, cudaStream_t s);
+
+cudaError_t launch_plan(const int32_t* seq_lens, int B, int max_pages, int page_size, int workers,
+                        int path, void* ws, const WorkspaceLayout& L, int32_t* dev_status,
+                        cudaStream_t s);
+cudaError_t launch_combine(const void* ws, const WorkspaceLayout& L, int B, int n_h, int d_c,
+                           float* o_lat, float* lse, cudaStream_t s);
+
+}  // namespace mla

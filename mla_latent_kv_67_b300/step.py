@@ -1,0 +1,129 @@
+"""One decode step of a workload, as the sequence of C-ABI calls.
+
+:class:`DecodeStep` uploads a workload's seeded inputs into device memory
+(torch only allocates), then :meth:`DecodeStep.run` enqueues the calls of one
+step on the current stream:
+
+  attn    : absorb_q -> plan -> decode_attn -> combine -> absorb_out
+  layer   : append_latent -> project_q -> absorb_q -> plan -> decode_attn
+            -> combine -> absorb_out -> out_proj
+  prefill : append_latent (all ctx tokens) -> project_q (last token) ->
+            absorb_q -> plan -> decode_attn -> combine -> absorb_out
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as M
+from . import synth
+
+
+def to_device(arr: np.ndarray, wl: synth.Workload, device) -> torch.Tensor:
+    """Storage-form numpy array -> device tensor (bf16 bits or float32)."""
+    if arr.dtype == np.uint16:
+        return torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(arr)).to(device)
+
+
+class DecodeStep:
+    def __init__(self, wl: synth.Workload, device="cuda", out_dtype=None):
+        self.wl, self.device = wl, torch.device(device)
+        self.dims = M.Dims.of(wl)
+        self.dtype = M.MLA_BF16 if wl.dtype == "bf16" else M.MLA_F32
+        tdt = M.torch_dtype(self.dtype)
+        dev = self.device
+        lens = synth.seq_lens(wl)
+        bt, pool = synth.block_table(wl, lens)
+        self.lens_np, self.bt_np, self.pool = lens, bt, pool
+        self.seq_lens = torch.from_numpy(lens).to(dev)
+        self.block_table = torch.from_numpy(bt).to(dev)
+        self.cache = to_device(synth.paged_cache(wl, lens, bt, pool), wl, dev)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        B, n_h = wl.batch, wl.n_h
+        W = lambda name: to_device(synth.storage(wl, synth.weight(wl, name)), wl, dev)
+        self.w_uk, self.w_uv = W("w_uk"), W("w_uv")
+        if wl.mode in ("layer", "prefill"):
+            self.w_dkv_kr = to_device(synth.storage(wl, synth.joint_w_dkv_kr(
+                synth.weight(wl, "w_dkv"), synth.weight(wl, "w_kr"))), wl, dev)
+            self.w_uq_qr = to_device(synth.storage(wl, synth.joint_w_uq_qr(
+                synth.weight(wl, "w_uq"), synth.weight(wl, "w_qr"), n_h)), wl, dev)
+            self.w_dq = W("w_dq") if wl.d_cq else None
+            self.x = to_device(synth.storage(wl, synth.tokens(wl)), wl, dev)
+            max_pos = int(lens.max())
+            self.rope = torch.empty((max_pos, wl.d_r // 2, 2), dtype=torch.float32, device=dev)
+            M.mla_rope_table(self.rope, wl.rope_base)
+            if wl.mode == "layer":
+                self.append_pos = (self.seq_lens - 1).contiguous()
+                self.append_seq = None
+                self.q_pos = self.append_pos
+                self.x_q = self.x
+            else:
+                self.append_pos = torch.arange(wl.ctx, dtype=torch.int32, device=dev)
+                self.append_seq = torch.zeros(wl.ctx, dtype=torch.int32, device=dev)
+                self.q_pos = self.append_pos[-1:].contiguous()
+                self.x_q = self.x[-1:].contiguous()
+            self.c_q = (torch.empty((B, wl.d_cq), dtype=tdt, device=dev) if wl.d_cq else None)
+            self.q = torch.empty((B, n_h, wl.d_h + wl.d_r), dtype=tdt, device=dev)
+            self.w_o = W("w_o") if wl.mode == "layer" else None
+        else:
+            self.q = to_device(synth.storage(wl, synth.query(wl)), wl, dev)
+        self.q_cat = torch.empty((B, n_h, wl.d_c + wl.d_r), dtype=tdt, device=dev)
+        ws = M.mla_decode_workspace_size(B, self.dtype, self.dims)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
+        self.o_lat = torch.empty((B, n_h, wl.d_c), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, n_h), dtype=torch.float32, device=dev)
+        if out_dtype is None:
+            out_dtype = tdt if wl.mode == "layer" else torch.float32
+        self.o = torch.empty((B, n_h * wl.d_v), dtype=out_dtype, device=dev)
+        self.u = (torch.empty((B, wl.d_model), dtype=torch.float32, device=dev)
+                  if wl.mode == "layer" else None)
+        self.max_pages = bt.shape[1]
+
+    # ------------------------------------------------------------- stages
+    def append(self):
+        M.mla_append_latent(self.x, self.w_dkv_kr, self.append_seq, self.append_pos,
+                            self.block_table, self.rope, self.cache, self.dims, self.dev_status)
+
+    def project(self):
+        M.mla_project_q(self.x_q, self.w_dq, self.w_uq_qr, self.q_pos, self.rope, self.c_q,
+                        self.q, self.dims, self.dev_status)
+
+    def absorb_q(self):
+        M.mla_absorb_q(self.q, self.w_uk, self.q_cat, self.dims)
+
+    def plan(self):
+        M.mla_plan_decode(self.seq_lens, self.max_pages, self.workspace, self.dtype, self.dims,
+                          self.dev_status)
+
+    def attend(self):
+        M.mla_decode_attn(self.q_cat, self.cache, self.block_table, self.seq_lens, self.wl.scale,
+                          self.workspace, self.o_lat, self.lse, self.dims, self.dev_status)
+
+    def combine(self):
+        M.mla_combine(self.workspace, self.o_lat, self.lse, self.dtype, self.dims)
+
+    def absorb_out(self):
+        M.mla_absorb_out(self.o_lat, self.w_uv, self.o, self.dims)
+
+    def out_proj(self):
+        M.mla_out_proj(self.o, self.w_o, self.u, self.dims)
+
+    def stages(self):
+        s = []
+        if self.wl.mode in ("layer", "prefill"):
+            s += [self.append, self.project]
+        s += [self.absorb_q, self.plan, self.attend, self.combine, self.absorb_out]
+        if self.wl.mode == "layer":
+            s.append(self.out_proj)
+        return s
+
+    def run(self):
+        for f in self.stages():
+            f()
+
+    def result(self) -> torch.Tensor:
+        return self.u if self.wl.mode == "layer" else self.o
+
+    def status(self) -> int:
+        return int(self.dev_status.item())

@@ -71,6 +71,7 @@ class Workload:
     seed: int = 67000
     shuffle_pages: bool = True
     spare_pages: int = 0
+    lens: tuple[int, ...] | None = None   # explicit per-sequence lengths
 
     @property
     def row_width(self) -> int:
@@ -138,6 +139,9 @@ def storage(wl: Workload, a: np.ndarray) -> np.ndarray:
 
 # ---------------------------------------------------------- lengths / paging
 def seq_lens(wl: Workload) -> np.ndarray:
+    if wl.lens is not None:
+        assert len(wl.lens) == wl.batch
+        return np.asarray(wl.lens, dtype=np.int32)
     if wl.ctx_range is None:
         return np.full(wl.batch, wl.ctx, dtype=np.int32)
     lo, hi = wl.ctx_range

@@ -1,0 +1,83 @@
+"""Expected values for a workload's sequences, computed by the fp64 oracle
+from the seeded inputs. Imports only ``oracle`` and ``synth`` (never the CUDA
+path)."""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import mla_oracle as O
+from mla_latent_kv_67_b300 import synth
+
+
+def rel_to_max(got, ref) -> float:
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+class Expected:
+    """Oracle inputs and outputs for one workload (weights drawn once)."""
+
+    def __init__(self, wl: synth.Workload):
+        self.wl = wl
+        self.lens = synth.seq_lens(wl)
+        self.w = {k: synth.weight(wl, k).astype(np.float64) for k in ("w_uk", "w_uv")}
+        if wl.mode in ("layer", "prefill"):
+            for k in ("w_dkv", "w_kr", "w_uq", "w_qr"):
+                self.w[k] = synth.weight(wl, k).astype(np.float64)
+            if wl.d_cq:
+                self.w["w_dq"] = synth.weight(wl, "w_dq").astype(np.float64)
+            if wl.mode == "layer":
+                self.w["w_o"] = synth.weight(wl, "w_o").astype(np.float64)
+            self.x = synth.tokens(wl).astype(np.float64)
+        else:
+            self.q = synth.query(wl).astype(np.float64)
+
+    def appended_rows(self, b: int):
+        """Rows the append step writes for sequence b: (positions, c, k_r)."""
+        wl = self.wl
+        if wl.mode == "layer":
+            pos = np.array([self.lens[b] - 1])
+            x = self.x[b:b + 1]
+        else:
+            pos = np.arange(wl.ctx)
+            x = self.x
+        c, k = O.latent_cache_row(x, self.w["w_dkv"], self.w["w_kr"], pos, wl.rope_base)
+        return pos, c, k
+
+    def query(self, b: int):
+        """(q_c [n_h, d_h], q_r [n_h, d_r]) of sequence b's decode token."""
+        wl = self.wl
+        if wl.mode == "attn":
+            return self.q[b, :, :wl.d_h], self.q[b, :, wl.d_h:]
+        x = self.x[b] if wl.mode == "layer" else self.x[-1]
+        pos = self.lens[b] - 1 if wl.mode == "layer" else wl.ctx - 1
+        return O.project_query(x, self.w["w_uq"], self.w["w_qr"], pos, wl.n_h,
+                               w_dq=self.w.get("w_dq"), base=wl.rope_base)
+
+    def cache_rows(self, b: int):
+        """(c [N, d_c], k_r [N, d_r]) of sequence b as the oracle sees them."""
+        wl = self.wl
+        n = int(self.lens[b])
+        nd = int(synth.drawn_rows(wl, self.lens)[b])
+        rows = synth.cache_rows(wl, b, nd).astype(np.float64)
+        c, k = rows[:, :wl.d_c], rows[:, wl.d_c:]
+        if nd < n:
+            _, c2, k2 = self.appended_rows(b)
+            c, k = np.concatenate([c, c2]), np.concatenate([k, k2])
+        return c, k
+
+    def seq(self, b: int, explicit_heads=None):
+        """Oracle outputs of sequence b: absorbed (all heads) and, for
+        ``explicit_heads``, the explicit non-absorbed definition."""
+        wl = self.wl
+        q_c, q_r = self.query(b)
+        c, k = self.cache_rows(b)
+        o, o_lat, lse = O.attention_absorbed(q_c, q_r, c, k, self.w["w_uk"], self.w["w_uv"], wl.scale)
+        out = dict(o=o, o_lat=o_lat, lse=lse, q_c=q_c, q_r=q_r)
+        if explicit_heads is not None:
+            oe, le = O.attention_explicit(q_c, q_r, c, k, self.w["w_uk"], self.w["w_uv"],
+                                          wl.scale, heads=explicit_heads)
+            out["o_explicit"], out["lse_explicit"] = oe, le
+        if wl.mode == "layer":
+            out["u"] = O.output_projection(o, self.w["w_o"])
+        return out
