@@ -75,13 +75,15 @@ def algorithmic(wl, lens):
 
 # --------------------------------------------------------------- clocks
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while running."""
+    """Samples SM clock and throttle reasons while the timed loop runs:
+    through NVML when the Python binding is importable, else by polling
+    ``nvidia-smi`` (read-only queries in both cases)."""
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
                0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index: int, period=0.02):
-        self.samples, self.reasons, self.period = [], set(), period
-        self.max_mhz = None
+        self.index, self.samples, self.reasons, self.period = index, [], set(), period
+        self.max_mhz, self.err, self.nv, self.proc = None, None, None, None
         self._stop = threading.Event()
         try:
             import pynvml
@@ -90,9 +92,9 @@ class ClockSampler:
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
         except Exception as e:  # noqa: BLE001
-            self.nv, self.err = None, str(e)
+            self.nv, self.err = None, f"nvml: {e}"
 
-    def _run(self):
+    def _run_nvml(self):
         while not self._stop.is_set():
             try:
                 self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
@@ -106,21 +108,51 @@ class ClockSampler:
 
     def __enter__(self):
         if self.nv:
-            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
+        else:
+            import subprocess
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception as e:  # noqa: BLE001
+                self.err = f"{self.err}; nvidia-smi: {e}"
         return self
 
     def __exit__(self, *a):
         self._stop.set()
         if self.nv:
             self.t.join()
+        elif self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
-        if not self.nv:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "error": self.err or "no samples"}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": "nvml" if self.nv else "nvidia-smi"}
 
 
 # ---------------------------------------------------------- CPU oracle
@@ -134,7 +166,9 @@ def cpu_oracle_sample(wl, target_s: float, seqs_heads=None):
     w_uk = synth.weight(wl, "w_uk").astype(np.float64)
     w_uv = synth.weight(wl, "w_uv").astype(np.float64)
     q = synth.query(wl).astype(np.float64)
-    pairs = seqs_heads or [(b, h) for h in range(0, wl.n_h, 16) for b in range(wl.batch)]
+    # heads in a spread order (0, 16, 32, ..., 1, 17, ...), sequences inner
+    order = [h0 + k for h0 in range(16) for k in range(0, wl.n_h, 16) if h0 + k < wl.n_h]
+    pairs = seqs_heads or [(b, h) for h in order for b in range(wl.batch)]
     spent, done, tok, rows_cache = 0.0, 0, 0, {}
     for b, h in pairs:
         if b not in rows_cache:
