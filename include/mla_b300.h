@@ -185,6 +185,35 @@ mla_status mla_absorb_out(const float* o_lat, const void* w_uv, void* o, int B, 
 mla_status mla_out_proj(const void* o, const void* w_o, float* u, int B, mla_dtype dtype,
                         const mla_dims* dims, void* stream);
 
+/* Allocation-free decode (the paper has no counterpart: this is a service
+ * for callers, not a step of the method). Some callers cannot allocate
+ * device memory when they decode -- code under a CUDA stream capture in
+ * global mode, where cudaMalloc is refused; plugin hosts and embedded
+ * runtimes that hand over a stream but no allocator; serving loops that ban
+ * driver allocations after start-up so no step blocks on the allocator --
+ * and so cannot supply the workspace mla_decode_attn needs. This call runs
+ * the same plan -> decode -> combine sequence with that workspace held in a
+ * file-scope device array of MLA_STATIC_SCRATCH_BYTES, which every GPU that
+ * loads this library keeps until the process exits. It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *   Arguments and outputs are those of mla_decode_attn (o_lat and lse are
+ *   final for every sequence; no mla_combine call follows).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call uses the same array and leaves its contents behind; nothing
+ *   in it has to start at zero. Calls that overlap on the GPU (other
+ *   streams, other host threads) race on it -- serialise them.
+ *   A batch whose plan and partials need more than MLA_STATIC_SCRATCH_BYTES
+ *   (see mla_decode_workspace_size) is refused with MLA_ERR_WORKSPACE before
+ *   anything is enqueued. */
+#define MLA_STATIC_SCRATCH_BYTES (48u << 20)
+mla_status mla_decode_attn_static(const void* q_cat, const void* cache,
+                                  const int32_t* block_table, int max_pages, int num_pages,
+                                  const int32_t* seq_lens, int B, float softmax_scale,
+                                  float* o_lat, float* lse, mla_dtype dtype,
+                                  const mla_dims* dims, int32_t* dev_status, void* stream);
+
 /* Which decode kernel the given dtype/dims select on the current device:
  * 1 = tcgen05 tensor-core kernel, 0 = CUDA-core (SIMT) kernel. */
 int mla_decode_path(mla_dtype dtype, const mla_dims* dims);

@@ -56,6 +56,7 @@ _SIGS = {
     "mla_plan_decode": (_I, [_P, _I, _I, _P, _S, _I, _DIMS, _P, _P]),
     "mla_decode_attn": (_I, [_P, _P, _P, _I, _I, _P, _I, _F, _P, _S, _P, _P, _I, _DIMS, _P, _P]),
     "mla_combine": (_I, [_P, _S, _I, _P, _P, _I, _DIMS, _P]),
+    "mla_decode_attn_static": (_I, [_P, _P, _P, _I, _I, _P, _I, _F, _P, _P, _I, _DIMS, _P, _P]),
     "mla_absorb_out": (_I, [_P, _P, _P, _I, _I, _I, _DIMS, _P]),
     "mla_out_proj": (_I, [_P, _P, _P, _I, _I, _DIMS, _P]),
 }
@@ -225,3 +226,19 @@ def mla_out_proj(o, w_o, u, dims: Dims, stream=None) -> None:
         _ptr(w_o, shape=(dims.d_model, dims.n_h * dims.d_v), name="w_o"),
         _ptr(u, torch.float32, (B, dims.d_model), "u"), B, _dt(w_o), ctypes.byref(dims),
         _stream(stream)))
+
+
+def mla_decode_attn_static(q_cat, cache, block_table, seq_lens, scale: float, o_lat, lse,
+                           dims: Dims, dev_status=None, stream=None) -> None:
+    """Plan, decode and combine with the library's static device scratch, for
+    callers that cannot allocate a workspace (see the header)."""
+    B, max_pages = block_table.shape
+    dt = _dt(cache)
+    _check(lib().mla_decode_attn_static(
+        _ptr(q_cat, cache.dtype, (B, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
+        _ptr(cache, shape=(cache.shape[0], dims.page_size, dims.d_c + dims.d_r), name="cache"),
+        _ptr(block_table, torch.int32, name="block_table"), max_pages, cache.shape[0],
+        _ptr(seq_lens, torch.int32, (B,), "seq_lens"), B, scale,
+        _ptr(o_lat, torch.float32, (B, dims.n_h, dims.d_c), "o_lat"),
+        _ptr(lse, torch.float32, (B, dims.n_h), "lse"), dt, ctypes.byref(dims),
+        _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))

@@ -76,6 +76,11 @@ cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 }  // namespace
 
+namespace mla {
+// Records `msg` as this host thread's mla_last_error() and returns `st`.
+mla_status record_error(mla_status st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace mla
+
 extern "C" {
 
 const char* mla_status_string(int st) {

@@ -49,4 +49,6 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int max_pages, int page_
 cudaError_t launch_combine(const void* ws, const WorkspaceLayout& L, int B, int n_h, int d_c,
                            float* o_lat, float* lse, cudaStream_t s);
 
+mla_status record_error(mla_status st, const char* msg);
+
 }  // namespace mla
