@@ -214,6 +214,17 @@ mla_status mla_decode_attn_static(const void* q_cat, const void* cache,
                                   float* o_lat, float* lse, mla_dtype dtype,
                                   const mla_dims* dims, int32_t* dev_status, void* stream);
 
+/* Diagnostic for the tensor-core decode kernel's data path (no counterpart
+ * in the method): one 64-token page through the same tcgen05 operand
+ * layouts, without softmax. All bf16 row-major device tensors:
+ *   q_cat [128][576], page [64][576], pmat [128][64];
+ *   s_out [128][64]  float = q_cat . page^T;
+ *   o_out [128][256] float = pmat . page[:, 256*half : 256*half + 256].
+ * Returns MLA_ERR_UNSUPPORTED on a device without the sm_103 tensor-core
+ * kernels. */
+mla_status mla_tc_selftest(const void* q_cat, const void* page, const void* pmat, float* s_out,
+                           float* o_out, int half, int32_t* dev_status, void* stream);
+
 /* Which decode kernel the given dtype/dims select on the current device:
  * 1 = tcgen05 tensor-core kernel, 0 = CUDA-core (SIMT) kernel. */
 int mla_decode_path(mla_dtype dtype, const mla_dims* dims);

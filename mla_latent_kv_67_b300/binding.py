@@ -58,6 +58,7 @@ _SIGS = {
     "mla_combine": (_I, [_P, _S, _I, _P, _P, _I, _DIMS, _P]),
     "mla_decode_attn_static": (_I, [_P, _P, _P, _I, _I, _P, _I, _F, _P, _P, _I, _DIMS, _P, _P]),
     "mla_absorb_out": (_I, [_P, _P, _P, _I, _I, _I, _DIMS, _P]),
+    "mla_tc_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "mla_out_proj": (_I, [_P, _P, _P, _I, _I, _DIMS, _P]),
 }
 
@@ -124,6 +125,17 @@ def mla_force_decode_path(path: int) -> None:
 
 def mla_decode_path(dtype: int, dims: Dims) -> int:
     return lib().mla_decode_path(dtype, ctypes.byref(dims))
+
+
+def mla_tc_selftest(q_cat, page, pmat, s_out, o_out, half: int, dev_status=None,
+                    stream=None) -> None:
+    """One page through the tensor-core decode data path (diagnostic)."""
+    bf = torch.bfloat16
+    _check(lib().mla_tc_selftest(
+        _ptr(q_cat, bf, (128, 576), "q_cat"), _ptr(page, bf, (64, 576), "page"),
+        _ptr(pmat, bf, (128, 64), "pmat"), _ptr(s_out, torch.float32, (128, 64), "s_out"),
+        _ptr(o_out, torch.float32, (128, 256), "o_out"), half,
+        _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
 
 
 def mla_rope_table(cos_sin: torch.Tensor, base: float = 10000.0, stream=None) -> None:

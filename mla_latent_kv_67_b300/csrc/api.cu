@@ -105,6 +105,16 @@ int mla_decode_path(mla_dtype dtype, const mla_dims* dims) {
   return pick_path(dtype, dims);
 }
 
+mla_status mla_tc_selftest(const void* q_cat, const void* page, const void* pmat, float* s_out,
+                           float* o_out, int half, int32_t* dev_status, void* stream) {
+  REQUIRE(q_cat && page && pmat && s_out && o_out, "NULL tensor argument");
+  REQUIRE(half == 0 || half == 1, "half must be 0 or 1");
+  if (!tc_decode_supported(128, 512, 64, 64))
+    return fail(MLA_ERR_UNSUPPORTED, "tensor-core decode kernel needs an sm_103 device");
+  return cuda_status(tc_selftest_launch(q_cat, page, pmat, s_out, o_out, half, dev_status, S(stream)),
+                     "tc_selftest");
+}
+
 mla_status mla_rope_table(float* cos_sin, int max_pos, int d_r, double base, void* stream) {
   REQUIRE(cos_sin != nullptr, "cos_sin is NULL");
   REQUIRE(max_pos >= 0 && d_r > 0 && d_r % 2 == 0, "bad max_pos=%d / d_r=%d", max_pos, d_r);

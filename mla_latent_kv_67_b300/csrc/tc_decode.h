@@ -19,4 +19,10 @@ cudaError_t tc_decode_launch(const void* q_cat, const void* cache, const int32_t
                              const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
                              int32_t* dev_status, cudaStream_t s);
 
+// One page of the decode's tensor-core data path without softmax:
+// s_out[128][64] = q_cat[128][576] . page[64][576]^T and
+// o_out[128][256] = pmat[128][64] . page[:, 256 r : 256 r + 256].
+cudaError_t tc_selftest_launch(const void* q_cat, const void* page, const void* pmat, float* s_out,
+                               float* o_out, int r, int32_t* dev_status, cudaStream_t s);
+
 }  // namespace mla
