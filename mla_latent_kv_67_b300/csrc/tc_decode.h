@@ -19,6 +19,20 @@ cudaError_t tc_decode_launch(const void* q_cat, const void* cache, const int32_t
                              const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
                              int32_t* dev_status, cudaStream_t s);
 
+// The CTA-pair kernel (score CTA + value CTA per worker).
+int tc_pair_workers(int sms);
+cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* block_table,
+                           int max_pages, int num_pages, int B, int workers, float scale,
+                           const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
+                           int32_t* dev_status, cudaStream_t s);
+
+// The split-page CTA-pair kernel (each CTA loads half of every page).
+int tc_split_workers(int sms);
+cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t* block_table,
+                            int max_pages, int num_pages, int workers, float scale, const void* ws,
+                            const WorkspaceLayout& L, float* o_lat, float* lse,
+                            int32_t* dev_status, cudaStream_t s);
+
 // One page of the decode's tensor-core data path without softmax:
 // s_out[128][64] = q_cat[128][576] . page[64][576]^T and
 // o_out[128][256] = pmat[128][64] . page[:, 256 r : 256 r + 256].

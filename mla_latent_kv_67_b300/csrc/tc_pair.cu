@@ -1,0 +1,735 @@
+// tcgen05 decode attention over the paged latent cache, one CTA pair per
+// worker (DeepSeek-V2 shapes: 128 heads, d_c = 512, d_R = 64, 64-token
+// pages, bf16).
+//
+// Per page the 128 heads of a sequence share every cached row, so the work
+// is two dense products on the 5th-generation tensor cores
+// ("DeepSeek-V2: Multi-Head Latent Attention (MLA) 原理与工程实现", 3.2: the
+// score is the latent-space content part plus the RoPE part; the latent
+// output is the probability-weighted sum of cached latents):
+//   S = Q_cat . Page^T      M = 128 heads, N = 64 tokens,  K = 576
+//   O += P . Page[:, 0:512] M = 128 heads, N = 512 latent, K = 64 tokens
+// The full O accumulator (128 x 512 fp32) fills all 512 columns of one SM's
+// tensor memory, so one SM cannot hold O together with Q and S. The two
+// products therefore run on the two CTAs (two SMs) of a cluster, each once:
+//
+//   rank 0, the score CTA: Q_cat in TMEM as the A operand, S into TMEM
+//     (double buffered), pages from a 3-stage ring; four softmax warps
+//     (thread = head row = TMEM lane) turn S into bf16 probabilities P and
+//     store them, with per-row rescale factors, straight from registers into
+//     the value CTA's shared memory (st.async, completion counted in bytes on
+//     the value CTA's barrier).
+//   rank 1, the value CTA: O in TMEM (all 512 columns), the pages' latent
+//     part from its own 2-stage ring, P from one of three slots; four
+//     epilogue warps apply rescales and write O / l.
+//
+// Each CTA loads its pages on its own: the second read of a page hits L2 and
+// costs no HBM bandwidth, and neither ring waits for the other. The MMA
+// issuers synchronise once per page (one barrier wait, one fence, one commit
+// per stage), since every such round trip costs about as much as several
+// MMAs.
+//
+// Online softmax: running maximum in log2 units; O is rescaled only when a
+// row's maximum grows by more than 8 (a factor 256). Until then P is taken
+// against the stale maximum, which stays exact because l uses the same
+// reference.
+//
+// Every mbarrier wait is bounded: after ~2 s it raises the CTA's abort flag
+// and the peer's, reports MLA_DEV_TIMEOUT, and both CTAs drain their copies
+// and MMAs and exit.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "launch.h"
+#include "sm100_ptx.cuh"
+#include "tc_decode.h"
+
+namespace mla {
+namespace tcp {
+
+using namespace ptx;
+
+constexpr int NH = 128, DC = 512, DR = 64, ROW = DC + DR, PAGE = 64;
+constexpr int NCHUNK = ROW / 64;  // 64-column (128-byte) chunks per cached row: 9
+constexpr int VCHUNK = DC / 64;   // latent chunks: 8
+constexpr uint32_t CHUNK = PAGE * 128;  // one chunk of a page: 64 tokens x 128 B
+constexpr int NKS = 3;                  // score CTA: page stages
+constexpr int NVS = 2;                  // value CTA: latent page stages
+constexpr int NP = 3;                   // P slots
+constexpr uint32_t KSTAGE = NCHUNK * CHUNK;
+constexpr uint32_t VSTAGE = VCHUNK * CHUNK;
+constexpr uint32_t P_BYTES = NH * 128;  // P [128][64] bf16, swizzled
+// per P slot: alpha[128], inv_l[128] (float), one rescale flag per softmax warp
+constexpr uint32_t XOFF_ALPHA = 0, XOFF_INVL = 4 * NH, XOFF_FLAG = 8 * NH;
+constexpr uint32_t X_BYTES = XOFF_FLAG + 16;
+constexpr uint32_t P_TX = P_BYTES + X_BYTES;  // bytes that fill one P slot
+
+// score CTA shared memory
+constexpr uint32_t S_OFF_K = 0;
+constexpr uint32_t S_OFF_BAR = S_OFF_K + NKS * KSTAGE;
+enum {
+  KFULL = 0,             // [NKS] page landed
+  KEMPTY = NKS,          // [NKS] page consumed by QK
+  SFULL = 2 * NKS,       // [2] S buffer written
+  SFREE = SFULL + 2,     // [2] S buffer read by the 4 softmax warps
+  QTMEM = SFREE + 2,     // Q of the segment in TMEM (4 warps)
+  QEMPTY = QTMEM + 1,    // last QK of a segment done
+  PEMPTY = QEMPTY + 1,   // [NP] value CTA done with P slot (4 remote warps)
+  SFINAL = PEMPTY + NP,  // drain after an abort
+  S_NBAR = SFINAL + 1
+};
+constexpr uint32_t S_OFF_TSLOT = S_OFF_BAR + 8 * S_NBAR;
+constexpr uint32_t S_OFF_ABORT = S_OFF_TSLOT + 4;
+constexpr uint32_t S_SMEM = S_OFF_ABORT + 4;
+
+// value CTA shared memory
+constexpr uint32_t V_OFF_V = 0;
+constexpr uint32_t V_OFF_P = V_OFF_V + NVS * VSTAGE;   // NP P slots
+constexpr uint32_t V_OFF_X = V_OFF_P + NP * P_BYTES;   // NP extras slots
+constexpr uint32_t V_OFF_BAR = V_OFF_X + NP * X_BYTES;
+enum {
+  VFULL = 0,            // [NVS] latent page landed
+  VEMPTY = NVS,         // [NVS] latent page consumed by PV
+  PFULL = 2 * NVS,      // [NP] P slot filled (armed here, bytes from the score CTA)
+  ODONE = PFULL + NP,   // [NP] PV from that P slot done
+  ORESC = ODONE + NP,   // O rescaled by the 4 epilogue warps
+  OFREE = ORESC + 1,    // O read out by the 4 epilogue warps
+  VFINAL = OFREE + 1,   // drain after an abort
+  V_NBAR = VFINAL + 1
+};
+constexpr uint32_t V_OFF_TSLOT = V_OFF_BAR + 8 * V_NBAR;
+constexpr uint32_t V_OFF_ABORT = V_OFF_TSLOT + 4;
+constexpr uint32_t V_SMEM = V_OFF_ABORT + 4;
+
+constexpr uint32_t SMEM_BYTES = S_SMEM > V_SMEM ? S_SMEM : V_SMEM;
+static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
+static_assert(V_OFF_P % 1024 == 0 && X_BYTES % 16 == 0 && V_OFF_BAR % 8 == 0, "layout alignment");
+
+// TMEM columns. Score CTA: S0 | S1 | Q (576 bf16 packed in 288 columns).
+constexpr uint32_t TM_S = 0, TM_Q = 128, TM_COLS = 512;
+
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 256, false, true);
+constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr uint64_t DRAIN_NS = 100000000ull;
+
+struct Params {
+  const __nv_bfloat16* q_cat;
+  const int32_t* block_table;
+  const char* ws;
+  WorkspaceLayout L;
+  float* o_lat;
+  float* lse;
+  int32_t* dev_status;
+  int max_pages, num_pages;
+  float scale_log2;
+};
+
+// A sequence's share of a worker's page range.
+struct Seg {
+  int s, p0, p1, len, slot;
+};
+
+__device__ __forceinline__ bool seg_at(const WorkerPlan& w, const SeqPlan* seqs, int g, int s,
+                                       Seg& out) {
+  const SeqPlan sp = seqs[s];
+  if (sp.pages == 0) return false;
+  const int p0 = s == w.seq_begin ? w.page_begin : 0;
+  const int p1 = s == w.seq_end ? w.page_end + 1 : sp.pages;
+  if (p0 >= p1) return false;
+  out.s = s;
+  out.p0 = p0;
+  out.p1 = p1;
+  out.len = sp.len;
+  out.slot = sp.n_splits > 1 ? sp.slot_begin + (g - sp.first_worker) : -1;
+  return true;
+}
+
+// First sequence at or after s0 in the worker's range that owns pages.
+__device__ __forceinline__ bool next_seg(const WorkerPlan& w, const SeqPlan* seqs, int g, int s0,
+                                         Seg& out) {
+  for (int s = s0; s <= w.seq_end; ++s)
+    if (seg_at(w, seqs, g, s, out)) return true;
+  return false;
+}
+
+struct Ctx {
+  uint32_t bar0;
+  volatile int* abort;
+  uint32_t peer_abort;  // cluster address of the peer's abort flag
+  int32_t* dev_status;
+  __device__ uint32_t bar(int i) const { return bar0 + 8u * (uint32_t)i; }
+  // Bounded waits; on failure also raise the peer's abort flag.
+  __device__ bool wait(int i, uint32_t parity) const {
+    if (mbar_wait_bounded(bar(i), parity, abort, dev_status, WAIT_NS)) return true;
+    st_cluster_u32(peer_abort, 1);
+    return false;
+  }
+  __device__ bool wait_cluster(int i, uint32_t parity) const {
+    if (mbar_wait_cluster_bounded(bar(i), parity, abort, dev_status, WAIT_NS)) return true;
+    st_cluster_u32(peer_abort, 1);
+    return false;
+  }
+};
+
+// Producer warp: for every page of the worker's range, in order, call
+// `issue(k, block)` on lane 0 (k = page count so far), and `on_seq(s)` on
+// lane 0 when sequence s starts. Lane-parallel block table reads; an
+// out-of-range block id is reported and replaced by page 0.
+template <typename F, typename G>
+__device__ __forceinline__ bool for_each_page(const Params& p, const WorkerPlan& w,
+                                              const SeqPlan* seqs, int g, int lane, F&& issue,
+                                              G&& on_seq) {
+  bool ok = true;
+  uint32_t k = 0;
+  for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
+    Seg sg;
+    if (!seg_at(w, seqs, g, s, sg)) continue;
+    if (lane == 0) on_seq(s);
+    for (int pb = sg.p0; ok && pb < sg.p1; pb += 32) {
+      int blk = 0;
+      if (pb + lane < sg.p1) {
+        blk = p.block_table[(size_t)s * p.max_pages + pb + lane];
+        if (blk < 0 || blk >= p.num_pages) {
+          report(p.dev_status, MLA_DEV_BAD_BLOCK);
+          blk = 0;
+        }
+      }
+      const int n = min(32, sg.p1 - pb);
+      for (int j = 0; ok && j < n; ++j, ++k) {
+        const int bk = __shfl_sync(0xffffffffu, blk, j);
+        if (lane == 0) ok = issue(k, bk);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+    }
+  }
+  return ok;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    tc_pair_decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t rank = cluster_ctarank();  // 0: score CTA, 1: value CTA
+  const uint32_t peer = rank ^ 1u;
+  const uint32_t sbase = smem_u32(smem);
+  Ctx cx;
+  cx.bar0 = sbase + (rank == 0 ? S_OFF_BAR : V_OFF_BAR);
+  cx.abort = reinterpret_cast<volatile int*>(smem + (rank == 0 ? S_OFF_ABORT : V_OFF_ABORT));
+  cx.peer_abort = mapa_shared(sbase + (rank == 0 ? V_OFF_ABORT : S_OFF_ABORT), peer);
+  cx.dev_status = p.dev_status;
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(smem + (rank == 0 ? S_OFF_TSLOT : V_OFF_TSLOT));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x >> 1;
+  const WorkerPlan w = reinterpret_cast<const WorkerPlan*>(p.ws + p.L.workers)[g];
+  const SeqPlan* seqs = reinterpret_cast<const SeqPlan*>(p.ws + p.L.seqs);
+  // Swizzled operand tiles need 1024-byte alignment of the shared window.
+  const bool aligned = (sbase & 1023u) == 0;
+
+  if (threadIdx.x == 0) {
+    if (rank == 0) {
+      for (int i = 0; i < NKS; ++i) {
+        mbar_init(cx.bar(KFULL + i), 1);
+        mbar_init(cx.bar(KEMPTY + i), 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(cx.bar(SFULL + i), 1);
+        mbar_init(cx.bar(SFREE + i), 4);
+      }
+      for (int i = 0; i < NP; ++i) mbar_init(cx.bar(PEMPTY + i), 4);
+      mbar_init(cx.bar(QTMEM), 4);
+      mbar_init(cx.bar(QEMPTY), 1);
+      mbar_init(cx.bar(SFINAL), 1);
+    } else {
+      for (int i = 0; i < NVS; ++i) {
+        mbar_init(cx.bar(VFULL + i), 1);
+        mbar_init(cx.bar(VEMPTY + i), 1);
+      }
+      for (int i = 0; i < NP; ++i) {
+        mbar_init(cx.bar(PFULL + i), 1);
+        mbar_init(cx.bar(ODONE + i), 1);
+        mbar_expect_tx(cx.bar(PFULL + i), P_TX);  // armed for the slot's first page
+      }
+      mbar_init(cx.bar(ORESC), 4);
+      mbar_init(cx.bar(OFREE), 4);
+      mbar_init(cx.bar(VFINAL), 1);
+    }
+    *cx.abort = 0;
+    if (!aligned) report(p.dev_status, MLA_DEV_TIMEOUT);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  cluster_sync_all();  // barriers of both CTAs initialised before any remote access
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool active = aligned && w.n_pages > 0;
+
+  if (active && rank == 0) {
+    // ============================================================ score CTA
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) tma_prefetch_desc(&tm_cache);
+      uint32_t issued = 0;
+      const bool ok = for_each_page(
+          p, w, seqs, g, lane,
+          [&](uint32_t k, int bk) -> bool {
+            const uint32_t st = k % NKS;
+            if (!cx.wait(KEMPTY + st, ((k / NKS) & 1) ^ 1)) return false;
+            mbar_expect_tx(cx.bar(KFULL + st), KSTAGE);
+            for (int c = 0; c < NCHUNK; ++c)
+              tma_load_2d(sbase + S_OFF_K + st * KSTAGE + c * CHUNK, &tm_cache, c * 64, bk * PAGE,
+                          cx.bar(KFULL + st));
+            issued = k + 1;
+            return true;
+          },
+          [&](int s) {  // the next sequence's Q rows into L2 for their TMEM load
+            if (s < w.seq_end) prefetch_l2(p.q_cat + (size_t)(s + 1) * NH * ROW, NH * ROW * 2);
+          });
+      if (!ok && lane == 0) {  // let issued copies land before the CTA exits
+        for (uint32_t k = issued > (uint32_t)NKS ? issued - NKS : 0; k < issued; ++k)
+          mbar_wait_drain(cx.bar(KFULL + k % NKS), (k / NKS) & 1, DRAIN_NS);
+      }
+    } else if (warp == 1) {
+      // --------------------------------------------------------- QK issue
+      if (lane == 0) {
+        uint32_t it = 0, seg = 0;
+        bool ok = true;
+        for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
+          Seg sg;
+          if (!seg_at(w, seqs, g, s, sg)) continue;
+          ok = cx.wait(QTMEM, seg & 1);
+          const int n = sg.p1 - sg.p0;
+          for (int j = 0; ok && j < n; ++j, ++it) {
+            const uint32_t sb = it & 1, st = it % NKS;
+            ok = cx.wait(SFREE + sb, ((it >> 1) & 1) ^ 1) && cx.wait(KFULL + st, (it / NKS) & 1);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t pg = sbase + S_OFF_K + st * KSTAGE;
+#pragma unroll
+            for (int kk = 0; kk < 4 * NCHUNK; ++kk)
+              mma_ts(tmem + TM_S + sb * 64, tmem + TM_Q + kk * 8,
+                     sdesc_sw128(pg + (kk >> 2) * CHUNK + (kk & 3) * 32, 16, 1024), IDESC_QK,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(cx.bar(KEMPTY + st));
+            mma_commit(cx.bar(SFULL + sb));
+          }
+          if (ok) mma_commit(cx.bar(QEMPTY));
+          ++seg;
+        }
+        if (!ok) {
+          mma_commit(cx.bar(SFINAL));
+          mbar_wait_drain(cx.bar(SFINAL), 0, DRAIN_NS);
+        }
+      }
+    } else {
+      // ---------------------------------------------------------- softmax
+      const int q4 = warp & 3;
+      const int row = q4 * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+      const uint32_t peer_pfull0 = mapa_shared(sbase + V_OFF_BAR + 8u * PFULL, peer);
+      const uint32_t peer_p0 = mapa_shared(sbase + V_OFF_P, peer);
+      const uint32_t peer_x0 = mapa_shared(sbase + V_OFF_X, peer);
+      float* lse_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.lse_part);
+      const float c = p.scale_log2;
+      // Q row of sequence qs into TMEM columns [TM_Q, TM_Q + 288)
+      auto load_q = [&](int qs) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + ((size_t)qs * NH + row) * ROW);
+#pragma unroll 1
+        for (int c0 = 0; c0 < NCHUNK; c0 += 3) {
+          uint4 x[24];
+#pragma unroll
+          for (int u = 0; u < 24; ++u) x[u] = __ldg(src + c0 * 8 + u);
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc) {
+            uint32_t v[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              v[4 * u] = x[8 * cc + u].x;
+              v[4 * u + 1] = x[8 * cc + u].y;
+              v[4 * u + 2] = x[8 * cc + u].z;
+              v[4 * u + 3] = x[8 * cc + u].w;
+            }
+            tmem_st32(lane_base + TM_Q + (c0 + cc) * 32, v);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cx.bar(QTMEM));
+      };
+      uint32_t it = 0, seg = 0;
+      bool ok = true;
+      Seg sg;
+      bool have = next_seg(w, seqs, g, w.seq_begin, sg);
+      if (have) load_q(sg.s);
+      for (; ok && have; ++seg) {
+        Seg nx;
+        const bool have_next = next_seg(w, seqs, g, sg.s + 1, nx);
+        float m = -INFINITY, l = 0.f;
+        const int n = sg.p1 - sg.p0;
+        for (int j = 0; j < n; ++j, ++it) {
+          const uint32_t sb = it & 1;
+          ok = __all_sync(0xffffffffu, cx.wait(SFULL + sb, (it >> 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t sa[32], sc[32];
+          tmem_ld32(lane_base + TM_S + sb * 64, sa);
+          tmem_ld32(lane_base + TM_S + sb * 64 + 32, sc);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(cx.bar(SFREE + sb));
+
+          const int nvalid = min(PAGE, sg.len - (sg.p0 + j) * PAGE);
+          if (nvalid < PAGE) {  // ragged tail: -inf scores give p = 0
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i >= nvalid) sa[i] = 0xff800000u;
+              if (32 + i >= nvalid) sc[i] = 0xff800000u;
+            }
+          }
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            mx[0] = fmaxf(mx[0], __uint_as_float(sa[i]));
+            mx[1] = fmaxf(mx[1], __uint_as_float(sa[i + 1]));
+            mx[2] = fmaxf(mx[2], __uint_as_float(sc[i]));
+            mx[3] = fmaxf(mx[3], __uint_as_float(sc[i + 1]));
+          }
+          const float mp = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
+          float m_use = m, alpha = 1.f;
+          bool resc = false;
+          if (j == 0) {
+            m_use = mp;
+          } else if (mp > m + 8.f) {
+            m_use = mp;
+            alpha = ex2_approx(m - mp);
+            resc = true;
+          }
+          const float nm = -m_use;
+          float sm[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float e0 = ex2_approx(fmaf(__uint_as_float(sa[2 * i]), c, nm));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(sa[2 * i + 1]), c, nm));
+            const float e2 = ex2_approx(fmaf(__uint_as_float(sc[2 * i]), c, nm));
+            const float e3 = ex2_approx(fmaf(__uint_as_float(sc[2 * i + 1]), c, nm));
+            sm[0] += e0;
+            sm[1] += e1;
+            sm[2] += e2;
+            sm[3] += e3;
+            pk[i] = pack_bf16x2(e0, e1);
+            pk[16 + i] = pack_bf16x2(e2, e3);
+          }
+          const float sum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+          l = (j == 0) ? sum : fmaf(l, alpha, sum);
+          m = m_use;
+          const bool last = j == n - 1;
+
+          // P row (and the row's rescale factor, 1 / l on the last page)
+          // straight into P slot it % NP of the value CTA
+          const uint32_t slot = it % NP;
+          ok = __all_sync(0xffffffffu, cx.wait_cluster(PEMPTY + slot, ((it / NP) & 1) ^ 1));
+          if (!ok) break;
+          const uint32_t pf = peer_pfull0 + 8u * slot;
+          const uint32_t prow = peer_p0 + slot * P_BYTES + row * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            st_async_v4(prow + ((u ^ (row & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                        pk[4 * u + 3], pf);
+          const uint32_t px = peer_x0 + slot * X_BYTES;
+          st_async_b32(px + XOFF_ALPHA + 4 * row, __float_as_uint(alpha), pf);
+          st_async_b32(px + XOFF_INVL + 4 * row, __float_as_uint(last ? 1.f / l : 0.f), pf);
+          const bool any_resc = __any_sync(0xffffffffu, resc);
+          if (lane == 0) st_async_b32(px + XOFF_FLAG + 4 * q4, any_resc ? 1u : 0u, pf);
+
+          // the next sequence's Q as soon as this one's last QK is done (the
+          // QK of its first page then overlaps the softmax of this last page)
+          if (have_next && j == (n >= 2 ? n - 2 : 0)) {
+            ok = __all_sync(0xffffffffu, cx.wait(QEMPTY, seg & 1));
+            if (!ok) break;
+            tc_fence_after();
+            load_q(nx.s);
+          }
+        }
+        if (!ok) break;
+        const float lse = (m + log2f(l)) * 0.69314718055994531f;
+        if (sg.slot < 0) p.lse[(size_t)sg.s * NH + row] = lse;
+        else lse_part[(size_t)sg.slot * NH + row] = lse;
+        sg = nx;
+        have = have_next;
+      }
+    }
+  } else if (active) {
+    // ============================================================ value CTA
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) tma_prefetch_desc(&tm_cache);
+      uint32_t issued = 0;
+      const bool ok = for_each_page(
+          p, w, seqs, g, lane,
+          [&](uint32_t k, int bk) -> bool {
+            const uint32_t st = k % NVS;
+            if (!cx.wait(VEMPTY + st, ((k / NVS) & 1) ^ 1)) return false;
+            mbar_expect_tx(cx.bar(VFULL + st), VSTAGE);
+            for (int c = 0; c < VCHUNK; ++c)
+              tma_load_2d(sbase + V_OFF_V + st * VSTAGE + c * CHUNK, &tm_cache, c * 64, bk * PAGE,
+                          cx.bar(VFULL + st));
+            issued = k + 1;
+            return true;
+          },
+          [](int) {});
+      if (!ok && lane == 0) {
+        for (uint32_t k = issued > (uint32_t)NVS ? issued - NVS : 0; k < issued; ++k)
+          mbar_wait_drain(cx.bar(VFULL + k % NVS), (k / NVS) & 1, DRAIN_NS);
+      }
+    } else if (warp == 1) {
+      // --------------------------------------------------------- PV issue
+      if (lane == 0) {
+        uint32_t it = 0, seg = 0, nres = 0;
+        bool ok = true;
+        for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
+          Seg sg;
+          if (!seg_at(w, seqs, g, s, sg)) continue;
+          const int n = sg.p1 - sg.p0;
+          for (int j = 0; ok && j < n; ++j, ++it) {
+            const uint32_t vs = it % NVS, slot = it % NP;
+            ok = cx.wait(VFULL + vs, (it / NVS) & 1) &&
+                 cx.wait_cluster(PFULL + slot, (it / NP) & 1) &&
+                 (j > 0 || seg == 0 || cx.wait(OFREE, (seg - 1) & 1));
+            if (!ok) break;
+            const volatile uint32_t* xf =
+                reinterpret_cast<const volatile uint32_t*>(smem + V_OFF_X + slot * X_BYTES + XOFF_FLAG);
+            if (xf[0] | xf[1] | xf[2] | xf[3]) {
+              ok = cx.wait(ORESC, nres & 1);
+              ++nres;
+              if (!ok) break;
+            }
+            tc_fence_after();
+            const uint32_t pa = sbase + V_OFF_P + slot * P_BYTES;
+            const uint32_t vb = sbase + V_OFF_V + vs * VSTAGE;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                mma_ss(tmem + h * 256, sdesc_sw128(pa + k * 32, 16, 1024),
+                       sdesc_sw128(vb + h * 4 * CHUNK + k * 2048, CHUNK, 1024), IDESC_PV,
+                       (j > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(cx.bar(VEMPTY + vs));
+            mma_commit(cx.bar(ODONE + slot));
+          }
+          ++seg;
+        }
+        if (!ok) {
+          mma_commit(cx.bar(VFINAL));
+          mbar_wait_drain(cx.bar(VFINAL), 0, DRAIN_NS);
+        }
+      }
+    } else {
+      // --------------------------------------------------------- epilogue
+      const int q4 = warp & 3;
+      const int row = q4 * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
+      const uint32_t peer_pempty0 = mapa_shared(sbase + S_OFF_BAR + 8u * PEMPTY, peer);
+      float* o_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.o_part);
+      // The slot's next page may now be stored: arm its barrier for the
+      // bytes (warp 0 of the four), then tell the score CTA.
+      auto release_slot = [&](uint32_t ps) {
+        if (lane == 0) {
+          if (q4 == 0) mbar_expect_tx(cx.bar(PFULL + ps), P_TX);
+          mbar_arrive_remote(peer_pempty0 + 8u * ps);
+        }
+      };
+      uint32_t it = 0;
+      bool ok = true;
+      for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
+        Seg sg;
+        if (!seg_at(w, seqs, g, s, sg)) continue;
+        const int n = sg.p1 - sg.p0;
+        float inv_l = 0.f;
+        for (int j = 0; j < n; ++j, ++it) {
+          if (j > 0) {  // PV of the previous page done: release its P slot
+            const uint32_t ps = (it - 1) % NP;
+            ok = __all_sync(0xffffffffu, cx.wait(ODONE + ps, ((it - 1) / NP) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            release_slot(ps);
+          }
+          const uint32_t slot = it % NP;
+          ok = __all_sync(0xffffffffu, cx.wait_cluster(PFULL + slot, (it / NP) & 1));
+          if (!ok) break;
+          const volatile uint8_t* xs = smem + V_OFF_X + slot * X_BYTES;
+          const volatile uint32_t* xf = reinterpret_cast<const volatile uint32_t*>(xs + XOFF_FLAG);
+          const uint32_t flags = xf[0] | xf[1] | xf[2] | xf[3];
+          if (j == n - 1) inv_l = reinterpret_cast<const volatile float*>(xs + XOFF_INVL)[row];
+          if (flags) {  // never on j == 0; O of the previous page is final
+            const float alpha = reinterpret_cast<const volatile float*>(xs + XOFF_ALPHA)[row];
+#pragma unroll 1
+            for (int cc = 0; cc < DC / 32; ++cc) {
+              uint32_t v[32];
+              tmem_ld32(lane_base + cc * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st32(lane_base + cc * 32, v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cx.bar(ORESC));
+          }
+        }
+        if (!ok) break;
+        // last PV of the segment done: release its slot, write O / l
+        const uint32_t ps = (it - 1) % NP;
+        ok = __all_sync(0xffffffffu, cx.wait(ODONE + ps, ((it - 1) / NP) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        release_slot(ps);
+        float* dst = sg.slot < 0 ? p.o_lat + ((size_t)sg.s * NH + row) * DC
+                                 : o_part + ((size_t)sg.slot * NH + row) * DC;
+#pragma unroll 1
+        for (int cc = 0; cc < DC / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + cc * 32, v);
+          tmem_ld_wait();
+          float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            d4[u] = make_float4(__uint_as_float(v[4 * u]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
+                                __uint_as_float(v[4 * u + 2]) * inv_l,
+                                __uint_as_float(v[4 * u + 3]) * inv_l);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cx.bar(OFREE));
+      }
+    }
+  }
+  __syncthreads();
+  if (*cx.abort) {
+    // stores this CTA sent to the peer complete on the peer's barriers; give
+    // any still in flight time to land before the cluster may exit
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TM_COLS);
+  }
+  cluster_sync_all();  // neither CTA leaves while the peer may still access it
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// The paged cache [num_pages * 64][576] bf16 as 2-D tiles of 64 rows x 64
+// columns with 128-byte swizzle.
+cudaError_t make_cache_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0) return cudaErrorMisalignedAddress;
+  const cuuint64_t dims[2] = {(cuuint64_t)ROW, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ROW * 2};
+  const cuuint32_t box[2] = {64, PAGE};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Clusters of two that can be resident at once on the current device with
+// this kernel's shared memory (0 if the query fails). Cached per device.
+int max_clusters() {
+  static int cached[64];
+  static bool have[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (have[dev]) return cached[dev];
+  if (cudaFuncSetAttribute(tc_pair_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)SMEM_BYTES) != cudaSuccess)
+    return 0;
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1));
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  int n = 0;
+  // The kernel's cluster shape is fixed at compile time; some runtimes also
+  // want it in the launch configuration.
+  if (cudaOccupancyMaxActiveClusters(&n, tc_pair_decode_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_pair_decode_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+  }
+  cached[dev] = n;
+  have[dev] = true;
+  return n;
+}
+
+}  // namespace tcp
+
+int tc_pair_workers(int sms) {
+  int n = sms / 2 > 0 ? sms / 2 : 1;
+  const int mc = tcp::max_clusters();
+  if (mc > 0 && mc < n) n = mc;
+  return n;
+}
+
+cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* block_table,
+                           int max_pages, int num_pages, int B, int workers, float scale,
+                           const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
+                           int32_t* dev_status, cudaStream_t s) {
+  (void)B;
+  CUtensorMap tm_cache;
+  cudaError_t e = tcp::make_cache_map(&tm_cache, cache, (uint64_t)num_pages * tcp::PAGE);
+  if (e != cudaSuccess) return e;
+  tcp::Params p;
+  p.q_cat = reinterpret_cast<const __nv_bfloat16*>(q_cat);
+  p.block_table = block_table;
+  p.ws = reinterpret_cast<const char*>(ws);
+  p.L = L;
+  p.o_lat = o_lat;
+  p.lse = lse;
+  p.dev_status = dev_status;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  e = cudaFuncSetAttribute(tcp::tc_pair_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tcp::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  tcp::tc_pair_decode_kernel<<<2 * workers, 192, tcp::SMEM_BYTES, s>>>(tm_cache, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla
