@@ -14,14 +14,17 @@
 // products therefore run on the two CTAs (two SMs) of a cluster, each once:
 //
 //   rank 0, the score CTA: Q_cat in TMEM as the A operand, S into TMEM
-//     (double buffered), pages from a 3-stage ring; four softmax warps
+//     (double buffered), pages from a 3-stage ring; two MMA issuer threads
+//     take even and odd pages (one issuer alone cannot keep the tensor core
+//     busy with 64-wide products); four softmax warps
 //     (thread = head row = TMEM lane) turn S into bf16 probabilities P and
 //     store them, with per-row rescale factors, straight from registers into
 //     the value CTA's shared memory (st.async, completion counted in bytes on
 //     the value CTA's barrier).
 //   rank 1, the value CTA: O in TMEM (all 512 columns), the pages' latent
 //     part from its own 2-stage ring, P from one of three slots; four
-//     epilogue warps apply rescales and write O / l.
+//     epilogue warps apply rescales and write O / l through a swizzled
+//     shared-memory transpose, so every warp store covers whole rows.
 //
 // Each CTA loads its pages on its own: the second read of a page hits L2 and
 // costs no HBM bandwidth, and neither ring waits for the other. The MMA
@@ -75,8 +78,9 @@ enum {
   QTMEM = SFREE + 2,     // Q of the segment in TMEM (4 warps)
   QEMPTY = QTMEM + 1,    // last QK of a segment done
   PEMPTY = QEMPTY + 1,   // [NP] value CTA done with P slot (4 remote warps)
-  SFINAL = PEMPTY + NP,  // drain after an abort
-  S_NBAR = SFINAL + 1
+  SFINAL = PEMPTY + NP,  // drain after an abort (issuer 0)
+  SFINAL2 = SFINAL + 1,  // drain after an abort (issuer 1)
+  S_NBAR = SFINAL2 + 1
 };
 constexpr uint32_t S_OFF_TSLOT = S_OFF_BAR + 8 * S_NBAR;
 constexpr uint32_t S_OFF_ABORT = S_OFF_TSLOT + 4;
@@ -86,7 +90,8 @@ constexpr uint32_t S_SMEM = S_OFF_ABORT + 4;
 constexpr uint32_t V_OFF_V = 0;
 constexpr uint32_t V_OFF_P = V_OFF_V + NVS * VSTAGE;   // NP P slots
 constexpr uint32_t V_OFF_X = V_OFF_P + NP * P_BYTES;   // NP extras slots
-constexpr uint32_t V_OFF_BAR = V_OFF_X + NP * X_BYTES;
+constexpr uint32_t V_OFF_STG = V_OFF_X + NP * X_BYTES;  // 4 warps x 32 rows x 128 B
+constexpr uint32_t V_OFF_BAR = V_OFF_STG + 4 * 32 * 128;
 enum {
   VFULL = 0,            // [NVS] latent page landed
   VEMPTY = NVS,         // [NVS] latent page consumed by PV
@@ -103,7 +108,8 @@ constexpr uint32_t V_SMEM = V_OFF_ABORT + 4;
 
 constexpr uint32_t SMEM_BYTES = S_SMEM > V_SMEM ? S_SMEM : V_SMEM;
 static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
-static_assert(V_OFF_P % 1024 == 0 && X_BYTES % 16 == 0 && V_OFF_BAR % 8 == 0, "layout alignment");
+static_assert(V_OFF_P % 1024 == 0 && X_BYTES % 16 == 0 && V_OFF_STG % 16 == 0 && V_OFF_BAR % 8 == 0,
+              "layout alignment");
 
 // TMEM columns. Score CTA: S0 | S1 | Q (576 bf16 packed in 288 columns).
 constexpr uint32_t TM_S = 0, TM_Q = 128, TM_COLS = 512;
@@ -206,7 +212,9 @@ __device__ __forceinline__ bool for_each_page(const Params& p, const WorkerPlan&
   return ok;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+constexpr int THREADS = 224;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_pair_decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t rank = cluster_ctarank();  // 0: score CTA, 1: value CTA
@@ -239,8 +247,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       }
       for (int i = 0; i < NP; ++i) mbar_init(cx.bar(PEMPTY + i), 4);
       mbar_init(cx.bar(QTMEM), 4);
-      mbar_init(cx.bar(QEMPTY), 1);
+      mbar_init(cx.bar(QEMPTY), 2);  // one commit per QK issuer
       mbar_init(cx.bar(SFINAL), 1);
+      mbar_init(cx.bar(SFINAL2), 1);
     } else {
       for (int i = 0; i < NVS; ++i) {
         mbar_init(cx.bar(VFULL + i), 1);
@@ -274,7 +283,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (warp == 0) {
       // ---------------------------------------------------------- producer
       if (lane == 0) tma_prefetch_desc(&tm_cache);
-      uint32_t issued = 0;
+      uint32_t issued = 0, q_prefetch_at = 0;
+      int q_prefetch_seq = -1;
       const bool ok = for_each_page(
           p, w, seqs, g, lane,
           [&](uint32_t k, int bk) -> bool {
@@ -285,48 +295,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
               tma_load_2d(sbase + S_OFF_K + st * KSTAGE + c * CHUNK, &tm_cache, c * 64, bk * PAGE,
                           cx.bar(KFULL + st));
             issued = k + 1;
+            if (k == q_prefetch_at && q_prefetch_seq >= 0)  // the next sequence's Q rows into L2
+              prefetch_l2(p.q_cat + (size_t)q_prefetch_seq * NH * ROW, NH * ROW * 2);
             return true;
           },
-          [&](int s) {  // the next sequence's Q rows into L2 for their TMEM load
-            if (s < w.seq_end) prefetch_l2(p.q_cat + (size_t)(s + 1) * NH * ROW, NH * ROW * 2);
+          [&](int s) {  // a few pages into sequence s, prefetch the next one's Q
+            q_prefetch_seq = s < w.seq_end ? s + 1 : -1;
+            q_prefetch_at = issued + 2;
           });
       if (!ok && lane == 0) {  // let issued copies land before the CTA exits
         for (uint32_t k = issued > (uint32_t)NKS ? issued - NKS : 0; k < issued; ++k)
           mbar_wait_drain(cx.bar(KFULL + k % NKS), (k / NKS) & 1, DRAIN_NS);
       }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 6) {
       // --------------------------------------------------------- QK issue
+      // issuer e = 0 (warp 1) takes even pages into S0, e = 1 (warp 6) odd
+      // pages into S1. Both wait for every sequence's Q (so neither can fall
+      // a phase behind) and arrive once per sequence on QEMPTY: by a commit
+      // after its last QK of the sequence, or a plain arrive if it had none
+      // (a commit with no new MMA since the thread's previous commit does not
+      // arrive).
       if (lane == 0) {
+        const uint32_t e = warp == 1 ? 0u : 1u;
         uint32_t it = 0, seg = 0;
         bool ok = true;
         for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
           Seg sg;
           if (!seg_at(w, seqs, g, s, sg)) continue;
-          ok = cx.wait(QTMEM, seg & 1);
           const int n = sg.p1 - sg.p0;
+          ok = cx.wait(QTMEM, seg & 1);
+          bool issued = false;
           for (int j = 0; ok && j < n; ++j, ++it) {
-            const uint32_t sb = it & 1, st = it % NKS;
-            ok = cx.wait(SFREE + sb, ((it >> 1) & 1) ^ 1) && cx.wait(KFULL + st, (it / NKS) & 1);
+            if ((it & 1) != e) continue;
+            const uint32_t st = it % NKS;
+            ok = cx.wait(SFREE + e, ((it >> 1) & 1) ^ 1) && cx.wait(KFULL + st, (it / NKS) & 1);
             if (!ok) break;
             tc_fence_after();
             const uint32_t pg = sbase + S_OFF_K + st * KSTAGE;
 #pragma unroll
             for (int kk = 0; kk < 4 * NCHUNK; ++kk)
-              mma_ts(tmem + TM_S + sb * 64, tmem + TM_Q + kk * 8,
+              mma_ts(tmem + TM_S + e * 64, tmem + TM_Q + kk * 8,
                      sdesc_sw128(pg + (kk >> 2) * CHUNK + (kk & 3) * 32, 16, 1024), IDESC_QK,
                      kk > 0 ? 1u : 0u);
             mma_commit(cx.bar(KEMPTY + st));
-            mma_commit(cx.bar(SFULL + sb));
+            mma_commit(cx.bar(SFULL + e));
+            issued = true;
           }
-          if (ok) mma_commit(cx.bar(QEMPTY));
+          if (ok) {
+            if (issued) mma_commit(cx.bar(QEMPTY));
+            else mbar_arrive(cx.bar(QEMPTY));
+          }
           ++seg;
         }
         if (!ok) {
-          mma_commit(cx.bar(SFINAL));
-          mbar_wait_drain(cx.bar(SFINAL), 0, DRAIN_NS);
+          mma_commit(cx.bar(SFINAL + e));
+          mbar_wait_drain(cx.bar(SFINAL + e), 0, DRAIN_NS);
         }
       }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
       // ---------------------------------------------------------- softmax
       const int q4 = warp & 3;
       const int row = q4 * 32 + lane;
@@ -532,7 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           mbar_wait_drain(cx.bar(VFINAL), 0, DRAIN_NS);
         }
       }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
       // --------------------------------------------------------- epilogue
       const int q4 = warp & 3;
       const int row = q4 * 32 + lane;
@@ -593,19 +619,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if (!ok) break;
         tc_fence_after();
         release_slot(ps);
-        float* dst = sg.slot < 0 ? p.o_lat + ((size_t)sg.s * NH + row) * DC
-                                 : o_part + ((size_t)sg.slot * NH + row) * DC;
+        // each warp owns rows [32 q4, 32 q4 + 32): per 32-column block, the
+        // thread of row r parks its 128 bytes in a swizzled staging tile,
+        // then each store instruction writes 4 whole 128-byte row pieces
+        float* dst0 = sg.slot < 0 ? p.o_lat + (size_t)sg.s * NH * DC
+                                  : o_part + (size_t)sg.slot * NH * DC;
+        uint8_t* stg = smem + V_OFF_STG + q4 * 32 * 128;
 #pragma unroll 1
         for (int cc = 0; cc < DC / 32; ++cc) {
           uint32_t v[32];
           tmem_ld32(lane_base + cc * 32, v);
           tmem_ld_wait();
-          float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            d4[u] = make_float4(__uint_as_float(v[4 * u]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
-                                __uint_as_float(v[4 * u + 2]) * inv_l,
-                                __uint_as_float(v[4 * u + 3]) * inv_l);
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(v[4 * u]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
+                            __uint_as_float(v[4 * u + 2]) * inv_l,
+                            __uint_as_float(v[4 * u + 3]) * inv_l);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3), u = lane & 7;
+            const float4 x = *reinterpret_cast<const float4*>(stg + r * 128 + ((u ^ (r & 7)) << 4));
+            *reinterpret_cast<float4*>(dst0 + (size_t)(q4 * 32 + r) * DC + cc * 32 + 4 * u) = x;
+          }
+          __syncwarp();
         }
         tc_fence_before();
         __syncwarp();
@@ -673,7 +711,7 @@ int max_clusters() {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1));
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   int n = 0;
   // The kernel's cluster shape is fixed at compile time; some runtimes also
@@ -728,7 +766,7 @@ cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* 
   e = cudaFuncSetAttribute(tcp::tc_pair_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)tcp::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  tcp::tc_pair_decode_kernel<<<2 * workers, 192, tcp::SMEM_BYTES, s>>>(tm_cache, p);
+  tcp::tc_pair_decode_kernel<<<2 * workers, tcp::THREADS, tcp::SMEM_BYTES, s>>>(tm_cache, p);
   return cudaGetLastError();
 }
 
