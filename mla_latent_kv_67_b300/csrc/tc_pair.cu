@@ -61,7 +61,11 @@ constexpr int NVS = 2;                  // value CTA: latent page stages
 constexpr int NP = 3;                   // P slots
 constexpr uint32_t KSTAGE = NCHUNK * CHUNK;
 constexpr uint32_t VSTAGE = VCHUNK * CHUNK;
-constexpr uint32_t P_BYTES = NH * 128;  // P [128][64] bf16, swizzled
+// P [128][64] bf16 in the non-swizzled core-matrix layout: the 16-byte
+// group u (tokens 8u..8u+7) of head row r sits at u * P_KGROUP + 16 r, so a
+// warp's store of one group covers 512 contiguous bytes.
+constexpr uint32_t P_BYTES = NH * 128;
+constexpr uint32_t P_KGROUP = NH * 16;
 // per P slot: alpha[128], inv_l[128] (float), one rescale flag per softmax warp
 constexpr uint32_t XOFF_ALPHA = 0, XOFF_INVL = 4 * NH, XOFF_FLAG = 8 * NH;
 constexpr uint32_t X_BYTES = XOFF_FLAG + 16;
@@ -464,11 +468,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ok = __all_sync(0xffffffffu, cx.wait_cluster(PEMPTY + slot, ((it / NP) & 1) ^ 1));
           if (!ok) break;
           const uint32_t pf = peer_pfull0 + 8u * slot;
-          const uint32_t prow = peer_p0 + slot * P_BYTES + row * 128;
+          const uint32_t prow = peer_p0 + slot * P_BYTES + row * 16;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            st_async_v4(prow + ((u ^ (row & 7)) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
-                        pk[4 * u + 3], pf);
+            st_async_v4(prow + u * P_KGROUP, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3],
+                        pf);
           const uint32_t px = peer_x0 + slot * X_BYTES;
           st_async_b32(px + XOFF_ALPHA + 4 * row, __float_as_uint(alpha), pf);
           st_async_b32(px + XOFF_INVL + 4 * row, __float_as_uint(last ? 1.f / l : 0.f), pf);
@@ -544,7 +548,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             for (int k = 0; k < 4; ++k) {
 #pragma unroll
               for (int h = 0; h < 2; ++h)
-                mma_ss(tmem + h * 256, sdesc_sw128(pa + k * 32, 16, 1024),
+                mma_ss(tmem + h * 256, sdesc_noswz(pa + k * 2 * P_KGROUP, P_KGROUP, 128),
                        sdesc_sw128(vb + h * 4 * CHUNK + k * 2048, CHUNK, 1024), IDESC_PV,
                        (j > 0 || k > 0) ? 1u : 0u);
             }
