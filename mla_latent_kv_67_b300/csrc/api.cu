@@ -201,6 +201,10 @@ mla_status mla_absorb_q(const void* q, const void* w_uk, void* q_cat, int B, mla
   if (B == 0) return MLA_OK;
   REQUIRE(q && w_uk && q_cat, "NULL tensor argument");
   const int f32 = dtype == MLA_F32;
+  if (!f32 && g_forced_path != 0 &&
+      tc_absorb_supported(dims->n_h, dims->d_h, dims->d_r, dims->d_c, dims->d_v))
+    return cuda_status(tc_absorb_q_launch(q, w_uk, q_cat, B, nullptr, S(stream)),
+                       "absorb_q (tcgen05)");
   const int qw = dims->d_h + dims->d_r, cw = dims->d_c + dims->d_r;
   GemmArgs g = {};
   g.a = q; g.a_gs = qw; g.a_ms = (long long)dims->n_h * qw; g.a_f32 = f32;
@@ -309,6 +313,11 @@ mla_status mla_absorb_out(const float* o_lat, const void* w_uv, void* o, int B, 
   REQUIRE(B >= 0, "B must be >= 0");
   if (B == 0) return MLA_OK;
   REQUIRE(o_lat && w_uv && o, "NULL tensor argument");
+  if (dtype == MLA_BF16 && g_forced_path != 0 &&
+      tc_absorb_supported(dims->n_h, dims->d_h, dims->d_r, dims->d_c, dims->d_v))
+    return cuda_status(tc_absorb_out_launch(o_lat, w_uv, o, out_dtype == MLA_F32, B, nullptr,
+                                            S(stream)),
+                       "absorb_out (tcgen05)");
   GemmArgs g = {};
   g.a = o_lat; g.a_gs = dims->d_c; g.a_ms = (long long)dims->n_h * dims->d_c; g.a_f32 = 1;
   g.w = w_uv; g.w_gs = (long long)dims->d_v * dims->d_c; g.w_ns = dims->d_c; g.w_ks = 1;

@@ -1,0 +1,314 @@
+// tcgen05 kernels for the two per-head absorption products of decode
+// ("DeepSeek-V2: Multi-Head Latent Attention (MLA) 原理与工程实现", 2.2: W^UK
+// folds into the query, W^UV maps the latent output back; DeepSeek-V2
+// shapes: 128 heads, d_h = d_v = 128, d_c = 512, d_R = 64, bf16 weights).
+//
+// Both are weight-streaming products with a small batch: every head's
+// weight block is read once, and the batch is the MMA's N dimension, so each
+// CTA computes D[128 x NT] = W-tile . X^T for one head and NT batch rows:
+//
+//   absorb_q:   q_cat[b, h, c] = sum_k q[b, h, k] W^UK[h*128 + k, c]
+//               A = W^UK_h^T (M = 128 latent columns c, K = 128, MN-major,
+//               straight from the row-major weight), B = q rows (K-major),
+//               one CTA per (128-column tile of c, head, batch tile). The
+//               RoPE part q_cat[b, h, 512:576] = q[b, h, 128:192] is copied
+//               by the first column tile.
+//   absorb_out: o[b, h*128 + v] = sum_c o_lat[b, h, c] W^UV[h*128 + v, c]
+//               A = W^UV_h (M = 128, K = 512, K-major), B = o_lat rows. The
+//               fp32 latent output is split into bf16 hi + lo parts (x = hi
+//               + lo to about 16 significant bits) and both are multiplied,
+//               so the tensor-core product keeps fp32-like input precision.
+//
+// Weights come in by TMA with 128-byte swizzle; activations by TMA (q) or
+// by the threads that split them (o_lat). fp32 accumulation in TMEM; one
+// thread issues the MMAs; all four warps run the epilogue (TMEM lane =
+// output row). Waits are bounded and report MLA_DEV_TIMEOUT.
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "sm100_ptx.cuh"
+#include "tc_decode.h"
+
+namespace mla {
+namespace tca {
+
+using namespace ptx;
+
+constexpr int NH = 128, DH = 128, DR = 64, DC = 512, DV = 128;
+constexpr int QW = DH + DR;   // q row width (192)
+constexpr int QC = DC + DR;   // q_cat row width (576)
+constexpr int NT = 32;        // batch rows per CTA
+constexpr uint64_t WAIT_NS = 2000000000ull;
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, int32_t* st) {
+  volatile int dummy = 0;
+  return mbar_wait_bounded(bar, parity, &dummy, st, WAIT_NS);
+}
+
+// ------------------------------------------------------------- absorb_q
+// smem: A0 | A1 (W^UK_h rows k, columns c0..c0+63 / c0+64..c0+127; 16 KB
+// each) | B0 | B1 (q rows, k 0..63 / 64..127; NT x 128 B each) | barriers.
+constexpr uint32_t AQ_A = 0, AQ_B = 2 * 16384, AQ_BAR = AQ_B + 2 * NT * 128;
+constexpr uint32_t AQ_SMEM = AQ_BAR + 64 + 1024;
+constexpr uint32_t IDESC_AQ = idesc_bf16_f32(128, NT, true, false);
+
+__global__ void __launch_bounds__(128)
+    absorb_q_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
+                    const __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ q_cat, int B,
+                    int32_t* dev_status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar_tma = sb + AQ_BAR, bar_mma = bar_tma + 8;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + AQ_BAR + 16);
+  const int mt = blockIdx.x, h = blockIdx.y, b0 = blockIdx.z * NT;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_tma, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tslot), 32);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(bar_tma, 2 * 16384 + 2 * NT * 128);
+    for (int i = 0; i < 2; ++i) {
+      tma_load_2d(sb + AQ_A + i * 16384, &tm_w, 128 * mt + 64 * i, DH * h, bar_tma);
+      tma_load_3d(sb + AQ_B + i * NT * 128, &tm_q, 64 * i, h, b0, bar_tma);
+    }
+    ok = wait_bar(bar_tma, 0, dev_status);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < DH / 16; ++kk)
+        mma_ss(tmem, sdesc_sw128(sb + AQ_A + kk * 2048, 16384, 1024),
+               sdesc_sw128(sb + AQ_B + (kk >> 2) * NT * 128 + (kk & 3) * 32, 16, 1024), IDESC_AQ,
+               kk > 0 ? 1u : 0u);
+    }
+    mma_commit(bar_mma);  // also drains on failure (no MMA issued then)
+  }
+  // RoPE part of q_cat, copied by the first column tile
+  if (mt == 0) {
+    for (int i = threadIdx.x; i < NT * 8; i += 128) {
+      const int r = i >> 3, u = i & 7;
+      if (b0 + r < B) {
+        const uint4 v = reinterpret_cast<const uint4*>(q + ((size_t)(b0 + r) * NH + h) * QW + DH)[u];
+        reinterpret_cast<uint4*>(q_cat + ((size_t)(b0 + r) * NH + h) * QC + DC)[u] = v;
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  const bool done = wait_bar(bar_mma, 0, dev_status);
+  if (ok && done) {
+    tc_fence_after();
+    uint32_t v[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), v);
+    tmem_ld_wait();
+    const int c = 128 * mt + 32 * warp + lane;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+      if (b0 + j < B) q_cat[((size_t)(b0 + j) * NH + h) * QC + c] = __float2bfloat16_rn(__uint_as_float(v[j]));
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
+// ----------------------------------------------------------- absorb_out
+// smem: A (W^UV_h, 8 chunks of 128 rows x 128 B = 128 KB) | B hi (8 chunks of
+// NT x 128 B) | B lo (same) | barriers.
+constexpr uint32_t AO_A = 0, AO_BHI = 8 * 16384, AO_BLO = AO_BHI + 8 * NT * 128;
+constexpr uint32_t AO_BAR = AO_BLO + 8 * NT * 128;
+constexpr uint32_t AO_SMEM = AO_BAR + 64 + 1024;
+constexpr uint32_t IDESC_AO = idesc_bf16_f32(128, NT, false, false);
+
+__global__ void __launch_bounds__(128)
+    absorb_out_kernel(const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ o_lat,
+                      void* __restrict__ o, int out_f32, int B, int32_t* dev_status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar_tma = sb + AO_BAR, bar_mma = bar_tma + 8;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + AO_BAR + 16);
+  const int h = blockIdx.x, b0 = blockIdx.y * NT;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_tma, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tslot), 32);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(bar_tma, 8 * 16384);
+    for (int c = 0; c < 8; ++c) tma_load_2d(sb + AO_A + c * 16384, &tm_w, 64 * c, DV * h, bar_tma);
+  }
+  // B: thread t splits row t / 4, latent chunks 2 (t % 4) and 2 (t % 4) + 1,
+  // into bf16 hi and lo parts, written in the 128-byte-swizzled K-major layout
+  {
+    const int r = threadIdx.x >> 2, cq = threadIdx.x & 3;
+    const bool valid = b0 + r < B;
+    const float4* src = reinterpret_cast<const float4*>(o_lat + ((size_t)(b0 + r) * NH + h) * DC);
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * cq + cc;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+        if (valid) {
+          x0 = __ldg(src + c * 16 + 2 * u);
+          x1 = __ldg(src + c * 16 + 2 * u + 1);
+        }
+        const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(xs[2 * e]), h1 = __float2bfloat16_rn(xs[2 * e + 1]);
+          hi[e] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
+          lo[e] = pack_bf16x2(xs[2 * e] - __bfloat162float(h0), xs[2 * e + 1] - __bfloat162float(h1));
+        }
+        const uint32_t off = c * NT * 128 + r * 128 + ((u ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(smem + AO_BHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + AO_BLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    ok = wait_bar(bar_tma, 0, dev_status);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int kk = 0; kk < DC / 16; ++kk) {
+        const uint32_t ka = sb + AO_A + (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t kb = (kk >> 2) * NT * 128 + (kk & 3) * 32;
+        mma_ss(tmem, sdesc_sw128(ka, 16, 1024), sdesc_sw128(sb + AO_BHI + kb, 16, 1024), IDESC_AO,
+               kk > 0 ? 1u : 0u);
+        mma_ss(tmem, sdesc_sw128(ka, 16, 1024), sdesc_sw128(sb + AO_BLO + kb, 16, 1024), IDESC_AO, 1u);
+      }
+    }
+    mma_commit(bar_mma);
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  const bool done = wait_bar(bar_mma, 0, dev_status);
+  if (ok && done) {
+    tc_fence_after();
+    uint32_t v[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), v);
+    tmem_ld_wait();
+    const int col = h * DV + 32 * warp + lane;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      if (b0 + j >= B) continue;
+      const size_t i = (size_t)(b0 + j) * NH * DV + col;
+      if (out_f32) reinterpret_cast<float*>(o)[i] = __uint_as_float(v[j]);
+      else reinterpret_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16_rn(__uint_as_float(v[j]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims/strides in elements/bytes.
+cudaError_t make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0) return cudaErrorMisalignedAddress;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult res = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace tca
+
+bool tc_absorb_supported(int n_h, int d_h, int d_r, int d_c, int d_v) {
+  return n_h == tca::NH && d_h == tca::DH && d_r == tca::DR && d_c == tca::DC && d_v == tca::DV &&
+         tc_decode_supported(n_h, d_c, d_r, 64);
+}
+
+cudaError_t tc_absorb_q_launch(const void* q, const void* w_uk, void* q_cat, int B,
+                               int32_t* dev_status, cudaStream_t s) {
+  CUtensorMap tm_w, tm_q;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)tca::DC, (cuuint64_t)tca::NH * tca::DH};
+    const cuuint64_t strides[1] = {(cuuint64_t)tca::DC * 2};
+    const cuuint32_t box[2] = {64, 128};
+    cudaError_t e = tca::make_map(&tm_w, w_uk, 2, dims, strides, box);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)tca::QW, (cuuint64_t)tca::NH, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {(cuuint64_t)tca::QW * 2, (cuuint64_t)tca::NH * tca::QW * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)tca::NT};
+    cudaError_t e = tca::make_map(&tm_q, q, 3, dims, strides, box);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaFuncSetAttribute(tca::absorb_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tca::AQ_SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(tca::DC / 128, tca::NH, (B + tca::NT - 1) / tca::NT);
+  tca::absorb_q_kernel<<<grid, 128, tca::AQ_SMEM, s>>>(
+      tm_w, tm_q, reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<__nv_bfloat16*>(q_cat), B,
+      dev_status);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_absorb_out_launch(const float* o_lat, const void* w_uv, void* o, int out_f32, int B,
+                                 int32_t* dev_status, cudaStream_t s) {
+  CUtensorMap tm_w;
+  const cuuint64_t dims[2] = {(cuuint64_t)tca::DC, (cuuint64_t)tca::NH * tca::DV};
+  const cuuint64_t strides[1] = {(cuuint64_t)tca::DC * 2};
+  const cuuint32_t box[2] = {64, 128};
+  cudaError_t e = tca::make_map(&tm_w, w_uv, 2, dims, strides, box);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tca::absorb_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)tca::AO_SMEM);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(tca::NH, (B + tca::NT - 1) / tca::NT);
+  tca::absorb_out_kernel<<<grid, 128, tca::AO_SMEM, s>>>(tm_w, o_lat, o, out_f32, B, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -33,6 +33,13 @@ cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t*
                             const WorkspaceLayout& L, float* o_lat, float* lse,
                             int32_t* dev_status, cudaStream_t s);
 
+// tcgen05 absorption products (DeepSeek-V2 shapes, bf16 weights).
+bool tc_absorb_supported(int n_h, int d_h, int d_r, int d_c, int d_v);
+cudaError_t tc_absorb_q_launch(const void* q, const void* w_uk, void* q_cat, int B,
+                               int32_t* dev_status, cudaStream_t s);
+cudaError_t tc_absorb_out_launch(const float* o_lat, const void* w_uv, void* o, int out_f32, int B,
+                                 int32_t* dev_status, cudaStream_t s);
+
 // One page of the decode's tensor-core data path without softmax:
 // s_out[128][64] = q_cat[128][576] . page[64][576]^T and
 // o_out[128][256] = pmat[128][64] . page[:, 256 r : 256 r + 256].
