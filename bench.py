@@ -11,7 +11,10 @@ through the C ABI. ``--workload`` picks another of the five workloads.
 Timing: W untimed warm-up steps, then K steps, each preceded by an L2 flush
 (a read of a buffer twice the L2 size, outside the timed events) and timed
 with CUDA events on the launching stream; barrier + synchronize on both sides
-of the timed loop; max over ranks. Inputs are resident in HBM. The ``e2e``
+of the timed loop; max over ranks. Inputs are resident in HBM. The step's
+calls are recorded once into a CUDA graph and ``value`` times its replays
+(the eager, call-by-call time is reported beside it); the decode kernel's
+own time comes from events around its call in the eager loop. The ``e2e``
 figure times the same step with the per-step inputs copied host->device from
 pinned memory and the result copied back, inside the timed region.
 
@@ -107,6 +110,7 @@ class ClockSampler:
             time.sleep(self.period)
 
     def __enter__(self):
+        self._stop.clear()
         if self.nv:
             self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
@@ -268,9 +272,11 @@ def main():
     def do_flush():
         flush.sum()
 
+    tc = M.mla_decode_path(st.dtype, st.dims) == 1
     launches_per_step = 0
     for f in st.stages():
-        launches_per_step += {"absorb_q": 2, "project": 2 if wl.d_cq else 1}.get(f.__name__, 1)
+        launches_per_step += {"absorb_q": 1 if tc else 2,
+                              "project": 2 if wl.d_cq else 1}.get(f.__name__, 1)
 
     def barrier():
         if world > 1:
@@ -282,6 +288,22 @@ def main():
         st.run()
     barrier()
     assert st.status() == 0, f"device status {st.status():#x}"
+
+    # The step's calls recorded once into a CUDA graph (the library allocates
+    # nothing and only enqueues work, so the calls capture as they are).
+    graph, graph_err = None, None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            st.run()
+        for _ in range(args.warmup):
+            do_flush()
+            g.replay()
+        barrier()
+        assert st.status() == 0, f"device status {st.status():#x}"
+        graph = g
+    except Exception as e:  # noqa: BLE001
+        graph_err = f"{type(e).__name__}: {e}"[:200]
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
@@ -306,6 +328,19 @@ def main():
         t_wall = time.perf_counter() - t_wall
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     attn_ms = sum(a.elapsed_time(b) for a, b in ka) / K
+    eager_ms = step_ms
+    if graph is not None:
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        with sampler:
+            barrier()
+            for i in range(K):
+                do_flush()
+                gev[i][0].record(stream)
+                graph.replay()
+                gev[i][1].record(stream)
+            barrier()
+        step_ms = sum(a.elapsed_time(b) for a, b in gev) / K
     if world > 1:
         t = torch.tensor([step_ms, attn_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -358,6 +393,8 @@ def main():
                    "d_r": wl.d_r, "page_size": wl.page_size,
                    "l2": f"flushed before every timed step (read of a {2 * l2 >> 20} MiB buffer, untimed)",
                    "decode_kernel": "tcgen05" if path == 1 else "simt",
+                   "step_launch": "cuda_graph" if graph is not None else f"eager ({graph_err})",
+                   "eager_us_per_step": eager_ms * 1e3,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm" if t_hbm >= t_flop else "tensor", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
@@ -370,7 +407,7 @@ def main():
                      "peak_source": peak_kind},
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches_per_step * K * (2 if graph is not None else 1),
         "clocks": sampler.summary(),
         "wall_s_timed": t_wall,
     }

@@ -62,17 +62,13 @@ int device_sms() {
 int pick_path(mla_dtype dt, const mla_dims* d) {
   if (g_forced_path == 0) return 0;
   const bool tc_ok = dt == MLA_BF16 && tc_decode_supported(d->n_h, d->d_c, d->d_r, d->page_size);
-  if (g_forced_path == 2) return tc_ok ? 2 : 0;
-  if (g_forced_path == 3) return tc_ok ? 3 : 0;
   return tc_ok ? 1 : 0;
 }
 
 int workers_for(int path) {
   const int sms = device_sms();
   if (sms <= 0) return 0;
-  if (path == 1) return tc_pair_workers(sms);
-  if (path == 3) return tc_split_workers(sms);
-  return path == 2 ? tc_decode_workers(sms) : sms;
+  return path == 1 ? tc_pair_workers(sms) : sms;
 }
 
 cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -102,7 +98,7 @@ const char* mla_last_error(void) { return g_last_error.c_str(); }
 int mla_abi_version(void) { return MLA_ABI_VERSION; }
 
 void mla_force_decode_path(int path) {
-  g_forced_path = (path >= 0 && path <= 3) ? path : -1;
+  g_forced_path = (path == 0 || path == 1) ? path : -1;
 }
 
 int mla_decode_path(mla_dtype dtype, const mla_dims* dims) {
@@ -270,16 +266,6 @@ mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* 
                                       workers, softmax_scale, workspace, L, o_lat, lse,
                                       dev_status, S(stream)),
                        "decode_attn (tcgen05 pair)");
-  if (path == 3)
-    return cuda_status(tc_split_launch(q_cat, cache, block_table, max_pages, num_pages,
-                                      workers, softmax_scale, workspace, L, o_lat, lse,
-                                      dev_status, S(stream)),
-                       "decode_attn (tcgen05 split pair)");
-  if (path == 2)
-    return cuda_status(tc_decode_launch(q_cat, cache, block_table, max_pages, num_pages, B,
-                                        workers, softmax_scale, workspace, L, o_lat, lse,
-                                        dev_status, S(stream)),
-                       "decode_attn (tcgen05)");
   return cuda_status(launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, B,
                                         workers, softmax_scale, workspace, L, o_lat, lse,
                                         dims->n_h, dims->d_c, dims->d_r, dims->page_size,

@@ -51,4 +51,17 @@ cudaError_t launch_combine(const void* ws, const WorkspaceLayout& L, int B, int 
 
 mla_status record_error(mla_status st, const char* msg);
 
+// Raises a kernel's dynamic shared-memory limit once per device, so later
+// launches (including ones recorded into a CUDA graph) make no further host
+// API call for it. `done` is the caller's per-kernel bit mask of devices.
+inline cudaError_t set_max_smem_once(const void* kernel, int bytes, unsigned long long& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && ((done >> dev) & 1ull)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < 64) done |= 1ull << dev;
+  return e;
+}
+
 }  // namespace mla

@@ -34,12 +34,16 @@ __device__ int block_inclusive_scan(int v, int* warp_sums) {
   return v;
 }
 
+constexpr int PLAN_SMEM_SEQS = 4096;  // sequences whose page starts stay in shared memory
+
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens, int B,
                                                     int max_pages, int page_size, int workers,
                                                     int path, char* ws, WorkspaceLayout L,
                                                     int32_t* dev_status) {
   __shared__ int warp_sums[32];
   __shared__ int carry_s;
+  __shared__ int begin_s[PLAN_SMEM_SEQS], pages_s[PLAN_SMEM_SEQS];
+  const bool in_smem = B <= PLAN_SMEM_SEQS;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws + L.header);
   SeqPlan* seqs = reinterpret_cast<SeqPlan*>(ws + L.seqs);
   WorkerPlan* wk = reinterpret_cast<WorkerPlan*>(ws + L.workers);
@@ -64,6 +68,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       seqs[b].page_begin = carry + incl - pages;
       seqs[b].pages = pages;
       seqs[b].len = len;
+      if (in_smem) {
+        begin_s[b] = carry + incl - pages;
+        pages_s[b] = pages;
+      }
     }
     __syncthreads();
     if (threadIdx.x == blockDim.x - 1) carry_s = carry + incl;
@@ -79,7 +87,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     const int b = base + threadIdx.x;
     int slots = 0;
     if (b < B) {
-      const int pb = seqs[b].page_begin, np = seqs[b].pages;
+      const int pb = in_smem ? begin_s[b] : seqs[b].page_begin;
+      const int np = in_smem ? pages_s[b] : seqs[b].pages;
       int first = 0, n = 0;
       if (np > 0) {
         first = pb / per;
@@ -115,10 +124,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         int lo = 0, hi = B - 1;
         while (lo < hi) {
           const int mid = (lo + hi + 1) >> 1;
-          if (seqs[mid].page_begin <= xs[e]) lo = mid; else hi = mid - 1;
+          const int bm = in_smem ? begin_s[mid] : seqs[mid].page_begin;
+          if (bm <= xs[e]) lo = mid; else hi = mid - 1;
         }
-        if (e == 0) { w.seq_begin = lo; w.page_begin = xs[e] - seqs[lo].page_begin; }
-        else        { w.seq_end = lo;   w.page_end = xs[e] - seqs[lo].page_begin; }
+        const int bl = in_smem ? begin_s[lo] : seqs[lo].page_begin;
+        if (e == 0) { w.seq_begin = lo; w.page_begin = xs[e] - bl; }
+        else        { w.seq_end = lo;   w.page_end = xs[e] - bl; }
       }
     }
     wk[g] = w;
@@ -133,40 +144,80 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
 }
 
-// One block per (sequence, head): merge the sequence's partial slots.
+// One warp per (sequence, head), four heads per block: merge the sequence's
+// partial slots, o = sum_s exp(lse_s - lse) o_s with lse = log sum_s
+// exp(lse_s). Each lane owns float4 columns lane, lane + 32, ... so every
+// load and store of the warp is one contiguous row piece.
 __global__ void __launch_bounds__(128) combine_kernel(const char* __restrict__ ws, WorkspaceLayout L,
                                                       int n_h, int d_c, float* __restrict__ o_lat,
                                                       float* __restrict__ lse) {
-  const int b = blockIdx.x, h = blockIdx.y;
+  const int b = blockIdx.x;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (h >= n_h) return;
   const SeqPlan sp = reinterpret_cast<const SeqPlan*>(ws + L.seqs)[b];
-  float* o = o_lat + ((size_t)b * n_h + h) * d_c;
   if (sp.n_splits == 1) return;  // written by the decode kernel
-  if (sp.n_splits == 0) {        // invalid length: defined, empty result
-    for (int c = threadIdx.x; c < d_c; c += blockDim.x) o[c] = 0.f;
-    if (threadIdx.x == 0) lse[(size_t)b * n_h + h] = -INFINITY;
+  float4* o = reinterpret_cast<float4*>(o_lat + ((size_t)b * n_h + h) * d_c);
+  const int n4 = d_c / 4;
+  if (sp.n_splits == 0) {  // invalid length: defined, empty result
+    for (int i = lane; i < n4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) lse[(size_t)b * n_h + h] = -INFINITY;
     return;
   }
   const float* lp = reinterpret_cast<const float*>(ws + L.lse_part);
   const float* op = reinterpret_cast<const float*>(ws + L.o_part);
+  // split weights: lane s reads split s's lse (32 at a time), warp max/sum
   float m = -INFINITY;
-  for (int s = 0; s < sp.n_splits; ++s) m = fmaxf(m, lp[(size_t)(sp.slot_begin + s) * n_h + h]);
+  for (int s0 = 0; s0 < sp.n_splits; s0 += 32) {
+    const float l = s0 + lane < sp.n_splits ? lp[(size_t)(sp.slot_begin + s0 + lane) * n_h + h] : -INFINITY;
+    m = fmaxf(m, l);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float z = 0.f;
-  for (int s = 0; s < sp.n_splits; ++s) {
-    const float l = lp[(size_t)(sp.slot_begin + s) * n_h + h];
+  for (int s0 = 0; s0 < sp.n_splits; s0 += 32) {
+    const float l = s0 + lane < sp.n_splits ? lp[(size_t)(sp.slot_begin + s0 + lane) * n_h + h] : -INFINITY;
     z += l == -INFINITY ? 0.f : expf(l - m);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
   const float inv = 1.f / z;
-  for (int c = threadIdx.x; c < d_c; c += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < sp.n_splits; ++s) {
-      const size_t slot = (size_t)(sp.slot_begin + s);
+  constexpr int MAXV = 4;  // float4 columns per lane held in registers (d_c <= 512)
+  float4 acc[MAXV];
+#pragma unroll
+  for (int v = 0; v < MAXV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // two splits per round, all their loads issued before any use
+  for (int s = 0; s < sp.n_splits; s += 2) {
+    float wgt[2];
+    float4 x[2][MAXV];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const bool have = s + t < sp.n_splits;
+      const size_t slot = (size_t)(sp.slot_begin + (have ? s + t : s));
       const float l = lp[slot * n_h + h];
-      if (l == -INFINITY) continue;
-      acc += expf(l - m) * op[(slot * n_h + h) * d_c + c];
+      wgt[t] = (have && l != -INFINITY) ? expf(l - m) * inv : 0.f;
+      const float4* src = reinterpret_cast<const float4*>(op + (slot * n_h + h) * d_c);
+#pragma unroll
+      for (int v = 0; v < MAXV; ++v) {
+        const int i = lane + 32 * v;
+        x[t][v] = (have && i < n4) ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-    o[c] = acc * inv;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int v = 0; v < MAXV; ++v) {
+        acc[v].x = fmaf(wgt[t], x[t][v].x, acc[v].x);
+        acc[v].y = fmaf(wgt[t], x[t][v].y, acc[v].y);
+        acc[v].z = fmaf(wgt[t], x[t][v].z, acc[v].z);
+        acc[v].w = fmaf(wgt[t], x[t][v].w, acc[v].w);
+      }
   }
-  if (threadIdx.x == 0) lse[(size_t)b * n_h + h] = m + logf(z);
+#pragma unroll
+  for (int v = 0; v < MAXV; ++v) {
+    const int i = lane + 32 * v;
+    if (i < n4) o[i] = acc[v];
+  }
+  if (lane == 0) lse[(size_t)b * n_h + h] = m + logf(z);
 }
 
 cudaError_t launch_plan(const int32_t* seq_lens, int B, int max_pages, int page_size, int workers,
@@ -180,7 +231,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int max_pages, int page_
 cudaError_t launch_combine(const void* ws, const WorkspaceLayout& L, int B, int n_h, int d_c,
                            float* o_lat, float* lse, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
-  combine_kernel<<<dim3(B, n_h), 128, 0, s>>>((const char*)ws, L, n_h, d_c, o_lat, lse);
+  combine_kernel<<<dim3(B, (n_h + 3) / 4), 128, 0, s>>>((const char*)ws, L, n_h, d_c, o_lat, lse);
   return cudaGetLastError();
 }
 

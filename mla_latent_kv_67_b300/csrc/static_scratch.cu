@@ -83,10 +83,7 @@ extern "C" mla_status mla_decode_attn_static(const void* q_cat, const void* cach
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return err(MLA_ERR_CUDA, "cannot query the device's SM count");
-  const int workers = path == 1   ? tc_pair_workers(sms)
-                      : path == 2 ? tc_decode_workers(sms)
-                      : path == 3 ? tc_split_workers(sms)
-                                  : sms;
+  const int workers = path == 1 ? tc_pair_workers(sms) : sms;
   const WorkspaceLayout L = workspace_layout(B, workers, d->n_h, d->d_c);
   if (L.total > (size_t)MLA_STATIC_SCRATCH_BYTES)
     return err(MLA_ERR_WORKSPACE,
@@ -106,12 +103,6 @@ extern "C" mla_status mla_decode_attn_static(const void* q_cat, const void* cach
     if (path == 1)
       e = tc_pair_launch(q_cat, cache, block_table, max_pages, num_pages, B, workers,
                          softmax_scale, ws, L, o_lat, lse, dev_status, s);
-    else if (path == 3)
-      e = tc_split_launch(q_cat, cache, block_table, max_pages, num_pages, workers,
-                          softmax_scale, ws, L, o_lat, lse, dev_status, s);
-    else if (path == 2)
-      e = tc_decode_launch(q_cat, cache, block_table, max_pages, num_pages, B, workers,
-                           softmax_scale, ws, L, o_lat, lse, dev_status, s);
     else
       e = launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, B, workers,
                              softmax_scale, ws, L, o_lat, lse, d->n_h, d->d_c, d->d_r,

@@ -285,8 +285,8 @@ cudaError_t tc_absorb_q_launch(const void* q, const void* w_uk, void* q_cat, int
     cudaError_t e = tca::make_map(&tm_q, q, 3, dims, strides, box);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(tca::absorb_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)tca::AQ_SMEM);
+  static unsigned long long smem_done = 0;
+  cudaError_t e = set_max_smem_once((const void*)tca::absorb_q_kernel, (int)tca::AQ_SMEM, smem_done);
   if (e != cudaSuccess) return e;
   const dim3 grid(tca::DC / 128, tca::NH, (B + tca::NT - 1) / tca::NT);
   tca::absorb_q_kernel<<<grid, 128, tca::AQ_SMEM, s>>>(
@@ -303,8 +303,8 @@ cudaError_t tc_absorb_out_launch(const float* o_lat, const void* w_uv, void* o, 
   const cuuint32_t box[2] = {64, 128};
   cudaError_t e = tca::make_map(&tm_w, w_uv, 2, dims, strides, box);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tca::absorb_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tca::AO_SMEM);
+  static unsigned long long smem_done = 0;
+  e = set_max_smem_once((const void*)tca::absorb_out_kernel, (int)tca::AO_SMEM, smem_done);
   if (e != cudaSuccess) return e;
   const dim3 grid(tca::NH, (B + tca::NT - 1) / tca::NT);
   tca::absorb_out_kernel<<<grid, 128, tca::AO_SMEM, s>>>(tm_w, o_lat, o, out_f32, B, dev_status);

@@ -708,8 +708,8 @@ int max_clusters() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (have[dev]) return cached[dev];
-  if (cudaFuncSetAttribute(tc_pair_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)SMEM_BYTES) != cudaSuccess)
+  static unsigned long long smem_done = 0;
+  if (set_max_smem_once((const void*)tc_pair_decode_kernel, (int)SMEM_BYTES, smem_done) != cudaSuccess)
     return 0;
   int sms = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -767,8 +767,8 @@ cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* 
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
-  e = cudaFuncSetAttribute(tcp::tc_pair_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)tcp::SMEM_BYTES);
+  static unsigned long long smem_done = 0;
+  e = set_max_smem_once((const void*)tcp::tc_pair_decode_kernel, (int)tcp::SMEM_BYTES, smem_done);
   if (e != cudaSuccess) return e;
   tcp::tc_pair_decode_kernel<<<2 * workers, tcp::THREADS, tcp::SMEM_BYTES, s>>>(tm_cache, p);
   return cudaGetLastError();
