@@ -59,6 +59,7 @@ constexpr uint32_t CHUNK = PAGE * 128;  // one chunk of a page: 64 tokens x 128 
 constexpr int NKS = 3;                  // score CTA: page stages
 constexpr int NVS = 2;                  // value CTA: latent page stages
 constexpr int NP = 3;                   // P slots
+constexpr int NSB = 3;                  // S buffers in TMEM
 constexpr uint32_t KSTAGE = NCHUNK * CHUNK;
 constexpr uint32_t VSTAGE = VCHUNK * CHUNK;
 // P [128][64] bf16 in the non-swizzled core-matrix layout: the 16-byte
@@ -77,9 +78,9 @@ constexpr uint32_t S_OFF_BAR = S_OFF_K + NKS * KSTAGE;
 enum {
   KFULL = 0,             // [NKS] page landed
   KEMPTY = NKS,          // [NKS] page consumed by QK
-  SFULL = 2 * NKS,       // [2] S buffer written
-  SFREE = SFULL + 2,     // [2] S buffer read by the 4 softmax warps
-  QTMEM = SFREE + 2,     // Q of the segment in TMEM (4 warps)
+  SFULL = 2 * NKS,       // [NSB] S buffer written
+  SFREE = SFULL + NSB,   // [NSB] S buffer read by the 4 softmax warps
+  QTMEM = SFREE + NSB,   // Q of the segment in TMEM (4 warps)
   QEMPTY = QTMEM + 1,    // last QK of a segment done
   PEMPTY = QEMPTY + 1,   // [NP] value CTA done with P slot (4 remote warps)
   SFINAL = PEMPTY + NP,  // drain after an abort (issuer 0)
@@ -115,8 +116,9 @@ static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 static_assert(V_OFF_P % 1024 == 0 && X_BYTES % 16 == 0 && V_OFF_STG % 16 == 0 && V_OFF_BAR % 8 == 0,
               "layout alignment");
 
-// TMEM columns. Score CTA: S0 | S1 | Q (576 bf16 packed in 288 columns).
-constexpr uint32_t TM_S = 0, TM_Q = 128, TM_COLS = 512;
+// TMEM columns. Score CTA: S0 | S1 | S2 | Q (576 bf16 packed in 288 columns).
+constexpr uint32_t TM_S = 0, TM_Q = 64 * NSB, TM_COLS = 512;
+static_assert(TM_Q + 288 <= TM_COLS, "score CTA TMEM budget");
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 256, false, true);
@@ -245,7 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         mbar_init(cx.bar(KFULL + i), 1);
         mbar_init(cx.bar(KEMPTY + i), 1);
       }
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < NSB; ++i) {
         mbar_init(cx.bar(SFULL + i), 1);
         mbar_init(cx.bar(SFREE + i), 4);
       }
@@ -331,18 +333,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           bool issued = false;
           for (int j = 0; ok && j < n; ++j, ++it) {
             if ((it & 1) != e) continue;
-            const uint32_t st = it % NKS;
-            ok = cx.wait(SFREE + e, ((it >> 1) & 1) ^ 1) && cx.wait(KFULL + st, (it / NKS) & 1);
+            const uint32_t st = it % NKS, sb = it % NSB;
+            ok = cx.wait(SFREE + sb, ((it / NSB) & 1) ^ 1) && cx.wait(KFULL + st, (it / NKS) & 1);
             if (!ok) break;
             tc_fence_after();
             const uint32_t pg = sbase + S_OFF_K + st * KSTAGE;
 #pragma unroll
             for (int kk = 0; kk < 4 * NCHUNK; ++kk)
-              mma_ts(tmem + TM_S + e * 64, tmem + TM_Q + kk * 8,
+              mma_ts(tmem + TM_S + sb * 64, tmem + TM_Q + kk * 8,
                      sdesc_sw128(pg + (kk >> 2) * CHUNK + (kk & 3) * 32, 16, 1024), IDESC_QK,
                      kk > 0 ? 1u : 0u);
             mma_commit(cx.bar(KEMPTY + st));
-            mma_commit(cx.bar(SFULL + e));
+            mma_commit(cx.bar(SFULL + sb));
             issued = true;
           }
           if (ok) {
@@ -403,8 +405,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         float m = -INFINITY, l = 0.f;
         const int n = sg.p1 - sg.p0;
         for (int j = 0; j < n; ++j, ++it) {
-          const uint32_t sb = it & 1;
-          ok = __all_sync(0xffffffffu, cx.wait(SFULL + sb, (it >> 1) & 1));
+          const uint32_t sb = it % NSB;
+          ok = __all_sync(0xffffffffu, cx.wait(SFULL + sb, (it / NSB) & 1));
           if (!ok) break;
           tc_fence_after();
           uint32_t sa[32], sc[32];
