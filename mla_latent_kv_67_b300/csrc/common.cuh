@@ -31,7 +31,7 @@ __device__ __forceinline__ void report(int32_t* dev_status, int bits) {
 // writes slot slot_begin + k.
 struct PlanHeader {
   int32_t workers;      // number of workers the plan was made for
-  int32_t per_worker;   // pages per worker (>= 1)
+  int32_t per_worker;   // cost units per worker (>= 1)
   int32_t total_pages;  // sum over sequences
   int32_t num_slots;    // partial slots used
   int32_t batch;
@@ -46,7 +46,8 @@ struct SeqPlan {
   int32_t n_splits;     // workers touching it
   int32_t slot_begin;   // first partial slot (valid if n_splits > 1)
   int32_t len;          // tokens (validated copy of seq_lens[b])
-  int32_t pad[2];
+  int32_t cost_begin;   // first cost unit (see plan_kernel)
+  int32_t pad;
 };
 
 struct WorkerPlan {

@@ -34,22 +34,29 @@ __device__ int block_inclusive_scan(int v, int* warp_sums) {
   return v;
 }
 
-constexpr int PLAN_SMEM_SEQS = 4096;  // sequences whose page starts stay in shared memory
+constexpr int PLAN_SMEM_SEQS = 4096;  // sequences whose cost prefix stays in shared memory
 
+// Work split. Every worker pays a fixed cost for each sequence it touches
+// (bringing the sequence's Q in, writing its partial O out) on top of one
+// unit per page. Each sequence with pages therefore gets `c_seg` cost units
+// in front of its pages, the cost axis is cut into `workers` equal ranges,
+// and worker g takes the pages whose units fall in its range: a worker that
+// starts a sequence inside its range gets c_seg pages fewer.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens, int B,
                                                     int max_pages, int page_size, int workers,
-                                                    int path, char* ws, WorkspaceLayout L,
+                                                    int path, int c_seg, char* ws, WorkspaceLayout L,
                                                     int32_t* dev_status) {
   __shared__ int warp_sums[32];
-  __shared__ int carry_s;
-  __shared__ int begin_s[PLAN_SMEM_SEQS], pages_s[PLAN_SMEM_SEQS];
+  __shared__ int carry_s, ccarry_s;
+  __shared__ int vend_s[PLAN_SMEM_SEQS], pages_s[PLAN_SMEM_SEQS];
   const bool in_smem = B <= PLAN_SMEM_SEQS;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(ws + L.header);
   SeqPlan* seqs = reinterpret_cast<SeqPlan*>(ws + L.seqs);
   WorkerPlan* wk = reinterpret_cast<WorkerPlan*>(ws + L.workers);
 
-  // pass 1: validated page counts and their exclusive prefix sum
-  if (threadIdx.x == 0) carry_s = 0;
+  // pass 1: validated page counts, their exclusive prefix sum, and the
+  // prefix sum of cost units (pages + c_seg per sequence with pages)
+  if (threadIdx.x == 0) carry_s = ccarry_s = 0;
   __syncthreads();
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
@@ -62,23 +69,31 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       }
       pages = (len + page_size - 1) / page_size;
     }
+    const int units = pages > 0 ? pages + c_seg : 0;
     const int incl = block_inclusive_scan(pages, warp_sums);
-    const int carry = carry_s;
+    const int cincl = block_inclusive_scan(units, warp_sums);
+    const int carry = carry_s, ccarry = ccarry_s;
     if (b < B) {
       seqs[b].page_begin = carry + incl - pages;
+      seqs[b].cost_begin = ccarry + cincl - units;
       seqs[b].pages = pages;
       seqs[b].len = len;
       if (in_smem) {
-        begin_s[b] = carry + incl - pages;
+        vend_s[b] = ccarry + cincl;
         pages_s[b] = pages;
       }
     }
     __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry_s = carry + incl;
+    if (threadIdx.x == blockDim.x - 1) {
+      carry_s = carry + incl;
+      ccarry_s = ccarry + cincl;
+    }
     __syncthreads();
   }
-  const int total = carry_s;
-  const int per = total > 0 ? (total + workers - 1) / workers : 1;
+  const int total = carry_s, total_units = ccarry_s;
+  const int per = total_units > 0 ? (total_units + workers - 1) / workers : 1;
+  auto vend = [&](int b) { return in_smem ? vend_s[b] : seqs[b].cost_begin + (seqs[b].pages > 0 ? seqs[b].pages + c_seg : 0); };
+  auto npages = [&](int b) { return in_smem ? pages_s[b] : seqs[b].pages; };
 
   // pass 2: which workers touch each sequence, and its partial slots
   if (threadIdx.x == 0) carry_s = 0;
@@ -87,12 +102,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     const int b = base + threadIdx.x;
     int slots = 0;
     if (b < B) {
-      const int pb = in_smem ? begin_s[b] : seqs[b].page_begin;
-      const int np = in_smem ? pages_s[b] : seqs[b].pages;
+      const int np = npages(b);
       int first = 0, n = 0;
       if (np > 0) {
-        first = pb / per;
-        n = (pb + np - 1) / per - first + 1;
+        const int rs = vend(b) - np;  // cost unit of the first page
+        first = rs / per;
+        n = (rs + np - 1) / per - first + 1;
       }
       seqs[b].first_worker = first;
       seqs[b].n_splits = n;
@@ -107,29 +122,45 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
   const int num_slots = carry_s;
 
-  // pass 3: each worker's (sequence, page) range, by binary search on
-  // page_begin (the last sequence whose first global page is <= x; a
-  // sequence with no pages shares its begin with the next one, so the
-  // search lands on a sequence that owns page x).
+  // pass 3: each worker's (sequence, page) range. Its units are [x0, x1];
+  // the first page is in the first sequence whose units end after x0 (it
+  // has pages: a sequence without pages ends where its predecessor does),
+  // the last in the last sequence with pages whose first page's unit is
+  // <= x1.
+  auto first_end_after = [&](int x) {  // smallest b with vend(b) > x, or B
+    int lo = 0, hi = B;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (vend(mid) > x) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+  };
   for (int g = threadIdx.x; g < workers; g += blockDim.x) {
     WorkerPlan w;
-    const int x0 = g * per;
-    const int x1 = min(x0 + per, total) - 1;  // inclusive
-    w.n_pages = x1 >= x0 ? x1 - x0 + 1 : 0;
-    w.seq_begin = w.page_begin = w.seq_end = w.page_end = 0;
+    w.seq_begin = w.page_begin = w.seq_end = w.page_end = w.n_pages = 0;
     w.pad[0] = w.pad[1] = w.pad[2] = 0;
-    if (w.n_pages > 0) {
-      int xs[2] = {x0, x1};
-      for (int e = 0; e < 2; ++e) {
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          const int bm = in_smem ? begin_s[mid] : seqs[mid].page_begin;
-          if (bm <= xs[e]) lo = mid; else hi = mid - 1;
+    const int x0 = g * per;
+    const int x1 = min(x0 + per, total_units) - 1;  // inclusive
+    if (x1 >= x0) {
+      const int bf = first_end_after(x0);
+      const int rsf = vend(bf) - npages(bf);
+      const int pf = max(0, x0 - rsf);
+      if (rsf + pf <= x1) {  // the range holds at least one page
+        int bl = first_end_after(x1);  // < B: the last sequence ends at total_units > x1
+        int pl;
+        const int rsl = vend(bl) - npages(bl);
+        if (rsl <= x1) {
+          pl = x1 - rsl;
+        } else {  // x1 falls in bl's leading units: the last page before them
+          bl -= 1;
+          while (bl > bf && npages(bl) == 0) --bl;
+          pl = npages(bl) - 1;
         }
-        const int bl = in_smem ? begin_s[lo] : seqs[lo].page_begin;
-        if (e == 0) { w.seq_begin = lo; w.page_begin = xs[e] - bl; }
-        else        { w.seq_end = lo;   w.page_end = xs[e] - bl; }
+        w.seq_begin = bf;
+        w.page_begin = pf;
+        w.seq_end = bl;
+        w.page_end = pl;
+        w.n_pages = (seqs[bl].page_begin + pl) - (seqs[bf].page_begin + pf) + 1;
       }
     }
     wk[g] = w;
@@ -223,8 +254,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const char* __restrict__ w
 cudaError_t launch_plan(const int32_t* seq_lens, int B, int max_pages, int page_size, int workers,
                         int path, void* ws, const WorkspaceLayout& L, int32_t* dev_status,
                         cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, B, max_pages, page_size, workers, path, (char*)ws, L,
-                                 dev_status);
+  // the tcgen05 kernel's per-sequence cost (Q fetch, O write-out) is worth
+  // about four pages; the SIMT kernel's is small next to its page cost
+  const int c_seg = path == 1 ? 4 : 0;
+  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, B, max_pages, page_size, workers, path, c_seg, (char*)ws,
+                                 L, dev_status);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Arrive `count` times at once (sm_90 and later).
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -64,6 +68,25 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         return false;
       }
     }
+  }
+}
+
+// For long waits of otherwise idle warps: poll every ~`sleep_ns` and sleep
+// in between, so the warps leave the issue slots to the busy ones. Bounded
+// like mbar_wait_bounded.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                 int32_t* dev_status, uint64_t limit_ns,
+                                                 uint32_t sleep_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      report(dev_status, MLA_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(sleep_ns);
   }
 }
 
@@ -124,6 +147,14 @@ __device__ __forceinline__ void cluster_sync_all() {
                    : "memory");
 }
 // Arrive on a barrier of another CTA of the cluster (address from mapa).
+// Commit to the barrier at shared offset `bar` in each CTA of `cta_mask`.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");

@@ -14,17 +14,29 @@
 // products therefore run on the two CTAs (two SMs) of a cluster, each once:
 //
 //   rank 0, the score CTA: Q_cat in TMEM as the A operand, S into TMEM
-//     (double buffered), pages from a 3-stage ring; two MMA issuer threads
+//     (three buffers), pages from a 3-stage ring; two MMA issuer threads
 //     take even and odd pages (one issuer alone cannot keep the tensor core
 //     busy with 64-wide products); four softmax warps
 //     (thread = head row = TMEM lane) turn S into bf16 probabilities P and
 //     store them, with per-row rescale factors, straight from registers into
 //     the value CTA's shared memory (st.async, completion counted in bytes on
-//     the value CTA's barrier).
+//     the value CTA's barrier). A sequence's Q_cat rows (128 x 576, the same
+//     shape as two pages) travel through the same ring as two items ahead of
+//     its pages, so the TMA engine fetches them and the softmax warps only
+//     move them from shared memory into TMEM.
 //   rank 1, the value CTA: O in TMEM (all 512 columns), the pages' latent
-//     part from its own 2-stage ring, P from one of three slots; four
-//     epilogue warps apply rescales and write O / l through a swizzled
-//     shared-memory transpose, so every warp store covers whole rows.
+//     part from its own 2-stage ring, P from one of three slots. The MMA
+//     issuer alone watches the P slots: it re-arms a slot's barrier, frees
+//     the slot with a commit straight to the score CTA's barrier, and hands
+//     the eight epilogue warps a command only when O needs work (a rescale,
+//     or a finished sequence). The epilogue warps sleep otherwise: every
+//     extra thread polling a barrier that 1,300 st.async completions per
+//     page also update slows the whole SM down. At a sequence's end the two
+//     groups of four write O / l, one 256-column half each, through a
+//     swizzled shared-memory transpose, so every warp store covers whole
+//     rows; each half is handed back to the next sequence's products as
+//     soon as it is written out. (One SM stores only ~50 GB/s, so the 256 KB
+//     of O take ~5 us however many warps write them.)
 //
 // Each CTA loads its pages on its own: the second read of a page hits L2 and
 // costs no HBM bandwidth, and neither ring waits for the other. The MMA
@@ -61,6 +73,7 @@ constexpr int NVS = 2;                  // value CTA: latent page stages
 constexpr int NP = 3;                   // P slots
 constexpr int NSB = 3;                  // S buffers in TMEM
 constexpr uint32_t KSTAGE = NCHUNK * CHUNK;
+constexpr int HALF_BLOCKS = DC / 2 / 32;  // 32-column TMEM blocks in one half of O
 constexpr uint32_t VSTAGE = VCHUNK * CHUNK;
 // P [128][64] bf16 in the non-swizzled core-matrix layout: the 16-byte
 // group u (tokens 8u..8u+7) of head row r sits at u * P_KGROUP + 16 r, so a
@@ -76,13 +89,13 @@ constexpr uint32_t P_TX = P_BYTES + X_BYTES;  // bytes that fill one P slot
 constexpr uint32_t S_OFF_K = 0;
 constexpr uint32_t S_OFF_BAR = S_OFF_K + NKS * KSTAGE;
 enum {
-  KFULL = 0,             // [NKS] page landed
-  KEMPTY = NKS,          // [NKS] page consumed by QK
+  KFULL = 0,             // [NKS] ring item (page or Q half) landed
+  KEMPTY = NKS,          // [NKS] ring item consumed (4 arrivals)
   SFULL = 2 * NKS,       // [NSB] S buffer written
   SFREE = SFULL + NSB,   // [NSB] S buffer read by the 4 softmax warps
   QTMEM = SFREE + NSB,   // Q of the segment in TMEM (4 warps)
   QEMPTY = QTMEM + 1,    // last QK of a segment done
-  PEMPTY = QEMPTY + 1,   // [NP] value CTA done with P slot (4 remote warps)
+  PEMPTY = QEMPTY + 1,   // [NP] value CTA done with P slot (its PV commit)
   SFINAL = PEMPTY + NP,  // drain after an abort (issuer 0)
   SFINAL2 = SFINAL + 1,  // drain after an abort (issuer 1)
   S_NBAR = SFINAL2 + 1
@@ -95,16 +108,21 @@ constexpr uint32_t S_SMEM = S_OFF_ABORT + 4;
 constexpr uint32_t V_OFF_V = 0;
 constexpr uint32_t V_OFF_P = V_OFF_V + NVS * VSTAGE;   // NP P slots
 constexpr uint32_t V_OFF_X = V_OFF_P + NP * P_BYTES;   // NP extras slots
-constexpr uint32_t V_OFF_STG = V_OFF_X + NP * X_BYTES;  // 4 warps x 32 rows x 128 B
-constexpr uint32_t V_OFF_BAR = V_OFF_STG + 4 * 32 * 128;
+constexpr uint32_t V_OFF_STG = V_OFF_X + NP * X_BYTES;  // 8 warps x 32 rows x 128 B
+constexpr uint32_t V_OFF_XA = V_OFF_STG + 8 * 32 * 128;  // alpha of a rescale command
+constexpr uint32_t V_OFF_XL = V_OFF_XA + 4 * NH;  // [2] 1 / l of a finished sequence (by its parity)
+constexpr uint32_t V_OFF_CMD = V_OFF_XL + 8 * NH;  // command: kind, page index
+constexpr uint32_t V_OFF_BAR = V_OFF_CMD + 16;
 enum {
   VFULL = 0,            // [NVS] latent page landed
   VEMPTY = NVS,         // [NVS] latent page consumed by PV
   PFULL = 2 * NVS,      // [NP] P slot filled (armed here, bytes from the score CTA)
   ODONE = PFULL + NP,   // [NP] PV from that P slot done
-  ORESC = ODONE + NP,   // O rescaled by the 4 epilogue warps
-  OFREE = ORESC + 1,    // O read out by the 4 epilogue warps
-  VFINAL = OFREE + 1,   // drain after an abort
+  ORESC = ODONE + NP,   // O rescaled by epilogue group 0
+  WORK = ORESC + 1,     // a command for epilogue group 0 (issuer)
+  EPI = WORK + 1,       // sequence finished (group 0 to group 1)
+  OFREE = EPI + 1,      // [2] a column half of O read out by its 4 warps
+  VFINAL = OFREE + 2,   // drain after an abort
   V_NBAR = VFINAL + 1
 };
 constexpr uint32_t V_OFF_TSLOT = V_OFF_BAR + 8 * V_NBAR;
@@ -126,7 +144,6 @@ constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 100000000ull;
 
 struct Params {
-  const __nv_bfloat16* q_cat;
   const int32_t* block_table;
   const char* ws;
   WorkspaceLayout L;
@@ -177,6 +194,11 @@ struct Ctx {
     st_cluster_u32(peer_abort, 1);
     return false;
   }
+  __device__ bool wait_sleepy(int i, uint32_t parity) const {
+    if (mbar_wait_sleepy(bar(i), parity, abort, dev_status, WAIT_NS, 256)) return true;
+    st_cluster_u32(peer_abort, 1);
+    return false;
+  }
   __device__ bool wait_cluster(int i, uint32_t parity) const {
     if (mbar_wait_cluster_bounded(bar(i), parity, abort, dev_status, WAIT_NS)) return true;
     st_cluster_u32(peer_abort, 1);
@@ -186,8 +208,9 @@ struct Ctx {
 
 // Producer warp: for every page of the worker's range, in order, call
 // `issue(k, block)` on lane 0 (k = page count so far), and `on_seq(s)` on
-// lane 0 when sequence s starts. Lane-parallel block table reads; an
-// out-of-range block id is reported and replaced by page 0.
+// lane 0 when sequence s starts; either returning false stops the walk.
+// Lane-parallel block table reads; an out-of-range block id is reported and
+// replaced by page 0.
 template <typename F, typename G>
 __device__ __forceinline__ bool for_each_page(const Params& p, const WorkerPlan& w,
                                               const SeqPlan* seqs, int g, int lane, F&& issue,
@@ -197,7 +220,8 @@ __device__ __forceinline__ bool for_each_page(const Params& p, const WorkerPlan&
   for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
     Seg sg;
     if (!seg_at(w, seqs, g, s, sg)) continue;
-    if (lane == 0) on_seq(s);
+    if (lane == 0) ok = on_seq(s);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
     for (int pb = sg.p0; ok && pb < sg.p1; pb += 32) {
       int blk = 0;
       if (pb + lane < sg.p1) {
@@ -218,10 +242,11 @@ __device__ __forceinline__ bool for_each_page(const Params& p, const WorkerPlan&
   return ok;
 }
 
-constexpr int THREADS = 224;
+constexpr int THREADS = 320;
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    tc_pair_decode_kernel(const __grid_constant__ CUtensorMap tm_cache, const Params p) {
+    tc_pair_decode_kernel(const __grid_constant__ CUtensorMap tm_cache,
+                          const __grid_constant__ CUtensorMap tm_q, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t rank = cluster_ctarank();  // 0: score CTA, 1: value CTA
   const uint32_t peer = rank ^ 1u;
@@ -245,13 +270,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (rank == 0) {
       for (int i = 0; i < NKS; ++i) {
         mbar_init(cx.bar(KFULL + i), 1);
-        mbar_init(cx.bar(KEMPTY + i), 1);
+        mbar_init(cx.bar(KEMPTY + i), 4);  // page: 3 + the QK commit; Q half: 2 warps x 2
       }
       for (int i = 0; i < NSB; ++i) {
         mbar_init(cx.bar(SFULL + i), 1);
         mbar_init(cx.bar(SFREE + i), 4);
       }
-      for (int i = 0; i < NP; ++i) mbar_init(cx.bar(PEMPTY + i), 4);
+      for (int i = 0; i < NP; ++i) mbar_init(cx.bar(PEMPTY + i), 1);
       mbar_init(cx.bar(QTMEM), 4);
       mbar_init(cx.bar(QEMPTY), 2);  // one commit per QK issuer
       mbar_init(cx.bar(SFINAL), 1);
@@ -267,7 +292,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         mbar_expect_tx(cx.bar(PFULL + i), P_TX);  // armed for the slot's first page
       }
       mbar_init(cx.bar(ORESC), 4);
+      mbar_init(cx.bar(WORK), 1);
+      mbar_init(cx.bar(EPI), 4);
       mbar_init(cx.bar(OFREE), 4);
+      mbar_init(cx.bar(OFREE + 1), 4);
       mbar_init(cx.bar(VFINAL), 1);
     }
     *cx.abort = 0;
@@ -288,29 +316,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ============================================================ score CTA
     if (warp == 0) {
       // ---------------------------------------------------------- producer
-      if (lane == 0) tma_prefetch_desc(&tm_cache);
-      uint32_t issued = 0, q_prefetch_at = 0;
-      int q_prefetch_seq = -1;
+      // ring items in order: per sequence its two Q halves (rows 0-63,
+      // 64-127 of Q_cat), then its pages
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_cache);
+        tma_prefetch_desc(&tm_q);
+      }
+      uint32_t rk = 0;  // ring items issued
+      auto put = [&](const CUtensorMap* map, int y) -> bool {
+        const uint32_t st = rk % NKS;
+        if (!cx.wait(KEMPTY + st, ((rk / NKS) & 1) ^ 1)) return false;
+        mbar_expect_tx(cx.bar(KFULL + st), KSTAGE);
+        for (int c = 0; c < NCHUNK; ++c)
+          tma_load_2d(sbase + S_OFF_K + st * KSTAGE + c * CHUNK, map, c * 64, y, cx.bar(KFULL + st));
+        ++rk;
+        return true;
+      };
       const bool ok = for_each_page(
-          p, w, seqs, g, lane,
-          [&](uint32_t k, int bk) -> bool {
-            const uint32_t st = k % NKS;
-            if (!cx.wait(KEMPTY + st, ((k / NKS) & 1) ^ 1)) return false;
-            mbar_expect_tx(cx.bar(KFULL + st), KSTAGE);
-            for (int c = 0; c < NCHUNK; ++c)
-              tma_load_2d(sbase + S_OFF_K + st * KSTAGE + c * CHUNK, &tm_cache, c * 64, bk * PAGE,
-                          cx.bar(KFULL + st));
-            issued = k + 1;
-            if (k == q_prefetch_at && q_prefetch_seq >= 0)  // the next sequence's Q rows into L2
-              prefetch_l2(p.q_cat + (size_t)q_prefetch_seq * NH * ROW, NH * ROW * 2);
-            return true;
-          },
-          [&](int s) {  // a few pages into sequence s, prefetch the next one's Q
-            q_prefetch_seq = s < w.seq_end ? s + 1 : -1;
-            q_prefetch_at = issued + 2;
-          });
+          p, w, seqs, g, lane, [&](uint32_t, int bk) -> bool { return put(&tm_cache, bk * PAGE); },
+          [&](int s) -> bool { return put(&tm_q, s * NH) && put(&tm_q, s * NH + PAGE); });
       if (!ok && lane == 0) {  // let issued copies land before the CTA exits
-        for (uint32_t k = issued > (uint32_t)NKS ? issued - NKS : 0; k < issued; ++k)
+        for (uint32_t k = rk > (uint32_t)NKS ? rk - NKS : 0; k < rk; ++k)
           mbar_wait_drain(cx.bar(KFULL + k % NKS), (k / NKS) & 1, DRAIN_NS);
       }
     } else if (warp == 1 || warp == 6) {
@@ -333,8 +359,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           bool issued = false;
           for (int j = 0; ok && j < n; ++j, ++it) {
             if ((it & 1) != e) continue;
-            const uint32_t st = it % NKS, sb = it % NSB;
-            ok = cx.wait(SFREE + sb, ((it / NSB) & 1) ^ 1) && cx.wait(KFULL + st, (it / NKS) & 1);
+            const uint32_t rk = it + 2 * (seg + 1);  // ring item: two Q halves per sequence so far
+            const uint32_t st = rk % NKS, sb = it % NSB;
+            ok = cx.wait(SFREE + sb, ((it / NSB) & 1) ^ 1) && cx.wait(KFULL + st, (rk / NKS) & 1);
             if (!ok) break;
             tc_fence_after();
             const uint32_t pg = sbase + S_OFF_K + st * KSTAGE;
@@ -343,6 +370,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               mma_ts(tmem + TM_S + sb * 64, tmem + TM_Q + kk * 8,
                      sdesc_sw128(pg + (kk >> 2) * CHUNK + (kk & 3) * 32, 16, 1024), IDESC_QK,
                      kk > 0 ? 1u : 0u);
+            mbar_arrive_cnt(cx.bar(KEMPTY + st), 3);  // the commit brings the fourth
             mma_commit(cx.bar(KEMPTY + st));
             mma_commit(cx.bar(SFULL + sb));
             issued = true;
@@ -368,42 +396,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t peer_x0 = mapa_shared(sbase + V_OFF_X, peer);
       float* lse_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.lse_part);
       const float c = p.scale_log2;
-      // Q row of sequence qs into TMEM columns [TM_Q, TM_Q + 288)
-      auto load_q = [&](int qs) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.q_cat + ((size_t)qs * NH + row) * ROW);
-#pragma unroll 1
-        for (int c0 = 0; c0 < NCHUNK; c0 += 3) {
-          uint4 x[24];
+      // This thread's Q_cat row from ring item rq (rows 0-63) or rq + 1
+      // (rows 64-127), un-swizzled, into TMEM columns [TM_Q, TM_Q + 288);
+      // the item's two warps then release it.
+      auto load_q = [&](uint32_t rq) -> bool {
+        const uint32_t k = rq + (uint32_t)(q4 >> 1), st = k % NKS;
+        if (!__all_sync(0xffffffffu, cx.wait(KFULL + st, (k / NKS) & 1))) return false;
+        const uint8_t* src = smem + S_OFF_K + st * KSTAGE + (row & 63) * 128;
+        const int sw = row & 7;
+#pragma unroll 3
+        for (int c = 0; c < NCHUNK; ++c) {
+          uint32_t v[32];
 #pragma unroll
-          for (int u = 0; u < 24; ++u) x[u] = __ldg(src + c0 * 8 + u);
-#pragma unroll
-          for (int cc = 0; cc < 3; ++cc) {
-            uint32_t v[32];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              v[4 * u] = x[8 * cc + u].x;
-              v[4 * u + 1] = x[8 * cc + u].y;
-              v[4 * u + 2] = x[8 * cc + u].z;
-              v[4 * u + 3] = x[8 * cc + u].w;
-            }
-            tmem_st32(lane_base + TM_Q + (c0 + cc) * 32, v);
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = *reinterpret_cast<const uint4*>(src + c * CHUNK + ((u ^ sw) << 4));
+            v[4 * u] = x.x;
+            v[4 * u + 1] = x.y;
+            v[4 * u + 2] = x.z;
+            v[4 * u + 3] = x.w;
           }
+          tmem_st32(lane_base + TM_Q + c * 32, v);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(cx.bar(QTMEM));
+        if (lane == 0) {
+          mbar_arrive_cnt(cx.bar(KEMPTY + st), 2);
+          mbar_arrive(cx.bar(QTMEM));
+        }
+        return true;
       };
       uint32_t it = 0, seg = 0;
-      bool ok = true;
       Seg sg;
       bool have = next_seg(w, seqs, g, w.seq_begin, sg);
-      if (have) load_q(sg.s);
+      bool ok = !have || load_q(0);
       for (; ok && have; ++seg) {
         Seg nx;
         const bool have_next = next_seg(w, seqs, g, sg.s + 1, nx);
         float m = -INFINITY, l = 0.f;
         const int n = sg.p1 - sg.p0;
+        const uint32_t rq_next = it + n + 2 * (seg + 1);  // ring item of the next sequence's Q
         for (int j = 0; j < n; ++j, ++it) {
           const uint32_t sb = it % NSB;
           ok = __all_sync(0xffffffffu, cx.wait(SFULL + sb, (it / NSB) & 1));
@@ -487,7 +519,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             ok = __all_sync(0xffffffffu, cx.wait(QEMPTY, seg & 1));
             if (!ok) break;
             tc_fence_after();
-            load_q(nx.s);
+            ok = load_q(rq_next);
+            if (!ok) break;
           }
         }
         if (!ok) break;
@@ -500,6 +533,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   } else if (active) {
     // ============================================================ value CTA
+    // O / l for column half `half` of a finished sequence (epilogue warps:
+    // warp w owns rows [32 (w % 4), 32 (w % 4) + 32)). Per 32-column block
+    // the thread of row r parks its 128 bytes in a swizzled staging tile,
+    // then each store instruction writes 4 whole 128-byte row pieces; the
+    // next block's TMEM load is in flight meanwhile. Arrives on OFREE + half.
+    auto write_half = [&](const Seg& sg, int half, float inv_l) {
+      const int q4 = warp & 3;
+      const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)half * (DC / 2);
+      float* o_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.o_part);
+      float* dst0 = (sg.slot < 0 ? p.o_lat + (size_t)sg.s * NH * DC
+                                 : o_part + (size_t)sg.slot * NH * DC) +
+                    half * (DC / 2);
+      uint8_t* stg = smem + V_OFF_STG + (warp - 2) * 32 * 128;
+      auto put_block = [&](int cc, const uint32_t (&v)[32]) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4*>(stg + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+              make_float4(__uint_as_float(v[4 * u]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
+                          __uint_as_float(v[4 * u + 2]) * inv_l,
+                          __uint_as_float(v[4 * u + 3]) * inv_l);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 4 * i + (lane >> 3), u = lane & 7;
+          const float4 x = *reinterpret_cast<const float4*>(stg + r * 128 + ((u ^ (r & 7)) << 4));
+          *reinterpret_cast<float4*>(dst0 + (size_t)(q4 * 32 + r) * DC + cc * 32 + 4 * u) = x;
+        }
+        __syncwarp();
+      };
+      uint32_t va[32], vb[32];
+      tmem_ld32(lane_base, va);
+#pragma unroll 1
+      for (int cc = 0; cc < HALF_BLOCKS; cc += 2) {
+        tmem_ld_wait();
+        tmem_ld32(lane_base + (cc + 1) * 32, vb);
+        put_block(cc, va);
+        tmem_ld_wait();
+        if (cc + 2 < HALF_BLOCKS) tmem_ld32(lane_base + (cc + 2) * 32, va);
+        put_block(cc + 1, vb);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(OFREE + half));
+    };
     if (warp == 0) {
       // ---------------------------------------------------------- producer
       if (lane == 0) tma_prefetch_desc(&tm_cache);
@@ -516,7 +593,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             issued = k + 1;
             return true;
           },
-          [](int) {});
+          [](int) { return true; });
       if (!ok && lane == 0) {
         for (uint32_t k = issued > (uint32_t)NVS ? issued - NVS : 0; k < issued; ++k)
           mbar_wait_drain(cx.bar(VFULL + k % NVS), (k / NVS) & 1, DRAIN_NS);
@@ -526,6 +603,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (lane == 0) {
         uint32_t it = 0, seg = 0, nres = 0;
         bool ok = true;
+        // 128 floats of a P slot's extras into a private copy
+        auto copy_rows = [&](uint32_t dst_off, const uint8_t* src) {
+#pragma unroll 4
+          for (int i = 0; i < NH / 4; ++i)
+            reinterpret_cast<uint4*>(smem + dst_off)[i] = reinterpret_cast<const uint4*>(src)[i];
+        };
+        // a command for epilogue group 0: kind 1 rescale before page it,
+        // kind 2 sequence finished with page it
+        auto post = [&](uint32_t kind, uint32_t page) {
+          volatile uint32_t* cmd = reinterpret_cast<volatile uint32_t*>(smem + V_OFF_CMD);
+          cmd[0] = kind;
+          cmd[1] = page;
+          mbar_arrive(cx.bar(WORK));
+        };
         for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
           Seg sg;
           if (!seg_at(w, seqs, g, s, sg)) continue;
@@ -533,29 +624,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           for (int j = 0; ok && j < n; ++j, ++it) {
             const uint32_t vs = it % NVS, slot = it % NP;
             ok = cx.wait(VFULL + vs, (it / NVS) & 1) &&
-                 cx.wait_cluster(PFULL + slot, (it / NP) & 1) &&
-                 (j > 0 || seg == 0 || cx.wait(OFREE, (seg - 1) & 1));
+                 cx.wait_cluster(PFULL + slot, (it / NP) & 1);
             if (!ok) break;
-            const volatile uint32_t* xf =
-                reinterpret_cast<const volatile uint32_t*>(smem + V_OFF_X + slot * X_BYTES + XOFF_FLAG);
-            if (xf[0] | xf[1] | xf[2] | xf[3]) {
+            mbar_expect_tx(cx.bar(PFULL + slot), P_TX);  // armed for the slot's next page
+            const uint8_t* xs = smem + V_OFF_X + slot * X_BYTES;
+            const uint32_t* xf = reinterpret_cast<const uint32_t*>(xs + XOFF_FLAG);
+            if (xf[0] | xf[1] | xf[2] | xf[3]) {  // never on j == 0
+              // rescale O by alpha (once PV of the previous page is done)
+              copy_rows(V_OFF_XA, xs + XOFF_ALPHA);
+              post(1u, it);
               ok = cx.wait(ORESC, nres & 1);
               ++nres;
               if (!ok) break;
             }
+            if (j == n - 1)  // before the slot is freed
+              copy_rows(V_OFF_XL + (seg & 1) * 4 * NH, xs + XOFF_INVL);
             tc_fence_after();
             const uint32_t pa = sbase + V_OFF_P + slot * P_BYTES;
             const uint32_t vb = sbase + V_OFF_V + vs * VSTAGE;
+            auto pv = [&](int k, int h) {
+              mma_ss(tmem + h * 256, sdesc_noswz(pa + k * 2 * P_KGROUP, P_KGROUP, 128),
+                     sdesc_sw128(vb + h * 4 * CHUNK + k * 2048, CHUNK, 1024), IDESC_PV,
+                     (j > 0 || k > 0) ? 1u : 0u);
+            };
+            if (j == 0 && seg > 0) {
+              // a sequence's first page: column half h of O once the previous
+              // sequence's half h has been written out
+              for (int h = 0; ok && h < 2; ++h) {
+                ok = cx.wait(OFREE + h, (seg - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < 4; ++k) pv(k, h);
+              }
+              if (!ok) break;
+            } else {
+              // alternate the two accumulators so consecutive products are
+              // independent
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
-                mma_ss(tmem + h * 256, sdesc_noswz(pa + k * 2 * P_KGROUP, P_KGROUP, 128),
-                       sdesc_sw128(vb + h * 4 * CHUNK + k * 2048, CHUNK, 1024), IDESC_PV,
-                       (j > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 4; ++k) {
+                pv(k, 0);
+                pv(k, 1);
+              }
             }
             mma_commit(cx.bar(VEMPTY + vs));
             mma_commit(cx.bar(ODONE + slot));
+            mma_commit_mc(sbase + S_OFF_BAR + 8u * (PEMPTY + slot), 1u);  // the score CTA's slot barrier
+            if (j == n - 1) post(2u, it);  // sequence finished
           }
           ++seg;
         }
@@ -565,95 +680,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
     } else if (warp >= 2 && warp <= 5) {
-      // --------------------------------------------------------- epilogue
+      // ------------------------------------------------ epilogue, group 0
+      // Sleeps until the issuer posts a command: rescale O (all 512
+      // columns) by alpha once PV of the page before is done, or, at a
+      // sequence's end, start group 1 and write O columns [0, 256).
       const int q4 = warp & 3;
       const int row = q4 * 32 + lane;
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
-      const uint32_t peer_pempty0 = mapa_shared(sbase + S_OFF_BAR + 8u * PEMPTY, peer);
-      float* o_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.o_part);
-      // The slot's next page may now be stored: arm its barrier for the
-      // bytes (warp 0 of the four), then tell the score CTA.
-      auto release_slot = [&](uint32_t ps) {
-        if (lane == 0) {
-          if (q4 == 0) mbar_expect_tx(cx.bar(PFULL + ps), P_TX);
-          mbar_arrive_remote(peer_pempty0 + 8u * ps);
+      const volatile uint32_t* cmd = reinterpret_cast<const volatile uint32_t*>(smem + V_OFF_CMD);
+      int nseg = 0;
+      for (int s = w.seq_begin; s <= w.seq_end; ++s) {
+        Seg sg;
+        if (seg_at(w, seqs, g, s, sg)) ++nseg;
+      }
+      Seg sg;
+      bool ok = nseg == 0 || next_seg(w, seqs, g, w.seq_begin, sg);
+      uint32_t ncmd = 0;
+      for (int done = 0; ok && done < nseg;) {
+        ok = __all_sync(0xffffffffu, cx.wait_sleepy(WORK, ncmd & 1));
+        if (!ok) break;
+        ++ncmd;
+        const uint32_t kind = cmd[0], page = cmd[1];
+        const uint32_t pd = kind == 1u ? page - 1 : page;  // page whose PV must be done
+        ok = __all_sync(0xffffffffu, cx.wait(ODONE + pd % NP, (pd / NP) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        if (kind == 1u) {
+          const float alpha = reinterpret_cast<const float*>(smem + V_OFF_XA)[row];
+#pragma unroll 1
+          for (int cc = 0; cc < DC / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + cc * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(lane_base + cc * 32, v);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(cx.bar(ORESC));
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(cx.bar(EPI));
+          write_half(sg, 0, reinterpret_cast<const float*>(smem + V_OFF_XL + (done & 1) * 4 * NH)[row]);
+          ++done;
+          if (done < nseg) ok = next_seg(w, seqs, g, sg.s + 1, sg);
         }
-      };
-      uint32_t it = 0;
+      }
+    } else if (warp >= 6 && warp <= 9) {
+      // ------------------------------------------------ epilogue, group 1
+      // At each sequence's end: O columns [256, 512).
+      const int row = (warp & 3) * 32 + lane;
+      const float* xl = reinterpret_cast<const float*>(smem + V_OFF_XL);
+      uint32_t seg = 0;
       bool ok = true;
       for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
         Seg sg;
         if (!seg_at(w, seqs, g, s, sg)) continue;
-        const int n = sg.p1 - sg.p0;
-        float inv_l = 0.f;
-        for (int j = 0; j < n; ++j, ++it) {
-          if (j > 0) {  // PV of the previous page done: release its P slot
-            const uint32_t ps = (it - 1) % NP;
-            ok = __all_sync(0xffffffffu, cx.wait(ODONE + ps, ((it - 1) / NP) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            release_slot(ps);
-          }
-          const uint32_t slot = it % NP;
-          ok = __all_sync(0xffffffffu, cx.wait_cluster(PFULL + slot, (it / NP) & 1));
-          if (!ok) break;
-          const volatile uint8_t* xs = smem + V_OFF_X + slot * X_BYTES;
-          const volatile uint32_t* xf = reinterpret_cast<const volatile uint32_t*>(xs + XOFF_FLAG);
-          const uint32_t flags = xf[0] | xf[1] | xf[2] | xf[3];
-          if (j == n - 1) inv_l = reinterpret_cast<const volatile float*>(xs + XOFF_INVL)[row];
-          if (flags) {  // never on j == 0; O of the previous page is final
-            const float alpha = reinterpret_cast<const volatile float*>(xs + XOFF_ALPHA)[row];
-#pragma unroll 1
-            for (int cc = 0; cc < DC / 32; ++cc) {
-              uint32_t v[32];
-              tmem_ld32(lane_base + cc * 32, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              tmem_st32(lane_base + cc * 32, v);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cx.bar(ORESC));
-          }
-        }
-        if (!ok) break;
-        // last PV of the segment done: release its slot, write O / l
-        const uint32_t ps = (it - 1) % NP;
-        ok = __all_sync(0xffffffffu, cx.wait(ODONE + ps, ((it - 1) / NP) & 1));
+        ok = __all_sync(0xffffffffu, cx.wait_sleepy(EPI, seg & 1));
         if (!ok) break;
         tc_fence_after();
-        release_slot(ps);
-        // each warp owns rows [32 q4, 32 q4 + 32): per 32-column block, the
-        // thread of row r parks its 128 bytes in a swizzled staging tile,
-        // then each store instruction writes 4 whole 128-byte row pieces
-        float* dst0 = sg.slot < 0 ? p.o_lat + (size_t)sg.s * NH * DC
-                                  : o_part + (size_t)sg.slot * NH * DC;
-        uint8_t* stg = smem + V_OFF_STG + q4 * 32 * 128;
-#pragma unroll 1
-        for (int cc = 0; cc < DC / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + cc * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<float4*>(stg + lane * 128 + ((u ^ (lane & 7)) << 4)) =
-                make_float4(__uint_as_float(v[4 * u]) * inv_l, __uint_as_float(v[4 * u + 1]) * inv_l,
-                            __uint_as_float(v[4 * u + 2]) * inv_l,
-                            __uint_as_float(v[4 * u + 3]) * inv_l);
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = 4 * i + (lane >> 3), u = lane & 7;
-            const float4 x = *reinterpret_cast<const float4*>(stg + r * 128 + ((u ^ (r & 7)) << 4));
-            *reinterpret_cast<float4*>(dst0 + (size_t)(q4 * 32 + r) * DC + cc * 32 + 4 * u) = x;
-          }
-          __syncwarp();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(cx.bar(OFREE));
+        write_half(sg, 1, xl[(seg & 1) * NH + row]);
+        ++seg;
       }
     }
   }
@@ -685,8 +775,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The paged cache [num_pages * 64][576] bf16 as 2-D tiles of 64 rows x 64
-// columns with 128-byte swizzle.
+// A [rows][576] bf16 array (the paged cache, or Q_cat) as 2-D tiles of 64
+// rows x 64 columns with 128-byte swizzle.
 cudaError_t make_cache_map(CUtensorMap* m, const void* base, uint64_t rows) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
@@ -754,12 +844,13 @@ cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* 
                            int max_pages, int num_pages, int B, int workers, float scale,
                            const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
                            int32_t* dev_status, cudaStream_t s) {
-  (void)B;
-  CUtensorMap tm_cache;
+  CUtensorMap tm_cache, tm_q;
   cudaError_t e = tcp::make_cache_map(&tm_cache, cache, (uint64_t)num_pages * tcp::PAGE);
   if (e != cudaSuccess) return e;
+  // Q_cat [B * 128][576] has the cache's row shape: the same tiling
+  e = tcp::make_cache_map(&tm_q, q_cat, (uint64_t)B * tcp::NH);
+  if (e != cudaSuccess) return e;
   tcp::Params p;
-  p.q_cat = reinterpret_cast<const __nv_bfloat16*>(q_cat);
   p.block_table = block_table;
   p.ws = reinterpret_cast<const char*>(ws);
   p.L = L;
@@ -772,7 +863,7 @@ cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* 
   static unsigned long long smem_done = 0;
   e = set_max_smem_once((const void*)tcp::tc_pair_decode_kernel, (int)tcp::SMEM_BYTES, smem_done);
   if (e != cudaSuccess) return e;
-  tcp::tc_pair_decode_kernel<<<2 * workers, tcp::THREADS, tcp::SMEM_BYTES, s>>>(tm_cache, p);
+  tcp::tc_pair_decode_kernel<<<2 * workers, tcp::THREADS, tcp::SMEM_BYTES, s>>>(tm_cache, tm_q, p);
   return cudaGetLastError();
 }
 
