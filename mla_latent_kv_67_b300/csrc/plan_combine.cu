@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 
@@ -196,52 +197,60 @@ __global__ void __launch_bounds__(128) combine_kernel(const char* __restrict__ w
   }
   const float* lp = reinterpret_cast<const float*>(ws + L.lse_part);
   const float* op = reinterpret_cast<const float*>(ws + L.o_part);
-  // split weights: lane s reads split s's lse (32 at a time), warp max/sum
-  float m = -INFINITY;
-  for (int s0 = 0; s0 < sp.n_splits; s0 += 32) {
-    const float l = s0 + lane < sp.n_splits ? lp[(size_t)(sp.slot_begin + s0 + lane) * n_h + h] : -INFINITY;
-    m = fmaxf(m, l);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float z = 0.f;
-  for (int s0 = 0; s0 < sp.n_splits; s0 += 32) {
-    const float l = s0 + lane < sp.n_splits ? lp[(size_t)(sp.slot_begin + s0 + lane) * n_h + h] : -INFINITY;
-    z += l == -INFINITY ? 0.f : expf(l - m);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  const float inv = 1.f / z;
+  const int n = sp.n_splits;
   constexpr int MAXV = 4;  // float4 columns per lane held in registers (d_c <= 512)
-  float4 acc[MAXV];
+  constexpr int RS = 4;    // splits whose rows are loaded per round
+  // One round: the rows of splits s0 .. s0 + RS - 1 (a split past the end
+  // re-reads the last one and gets weight 0), all loads issued together.
+  float4 x[RS][MAXV];
+  auto load_round = [&](int s0) {
 #pragma unroll
-  for (int v = 0; v < MAXV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  // two splits per round, all their loads issued before any use
-  for (int s = 0; s < sp.n_splits; s += 2) {
-    float wgt[2];
-    float4 x[2][MAXV];
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const bool have = s + t < sp.n_splits;
-      const size_t slot = (size_t)(sp.slot_begin + (have ? s + t : s));
-      const float l = lp[slot * n_h + h];
-      wgt[t] = (have && l != -INFINITY) ? expf(l - m) * inv : 0.f;
+    for (int t = 0; t < RS; ++t) {
+      const size_t slot = (size_t)(sp.slot_begin + min(s0 + t, n - 1));
       const float4* src = reinterpret_cast<const float4*>(op + (slot * n_h + h) * d_c);
 #pragma unroll
       for (int v = 0; v < MAXV; ++v) {
         const int i = lane + 32 * v;
-        x[t][v] = (have && i < n4) ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[t][v] = i < n4 ? ptx::ld_nc_v4(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
+  };
+  // the first round's rows and the splits' lse values in flight together
+  load_round(0);
+  const float l_lane = lane < n ? lp[(size_t)(sp.slot_begin + lane) * n_h + h] : -INFINITY;
+  float m = l_lane;
+  for (int s0 = 32; s0 < n; s0 += 32)  // more than 32 splits: rare
+    if (s0 + lane < n) m = fmaxf(m, lp[(size_t)(sp.slot_begin + s0 + lane) * n_h + h]);
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float z = l_lane == -INFINITY ? 0.f : expf(l_lane - m);
+  for (int s0 = 32; s0 < n; s0 += 32)
+    if (s0 + lane < n) {
+      const float l = lp[(size_t)(sp.slot_begin + s0 + lane) * n_h + h];
+      z += l == -INFINITY ? 0.f : expf(l - m);
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  const float inv = 1.f / z;
+  float4 acc[MAXV];
+#pragma unroll
+  for (int v = 0; v < MAXV; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < n; s0 += RS) {
+    if (s0 > 0) load_round(s0);
+#pragma unroll
+    for (int t = 0; t < RS; ++t) {
+      const int sidx = s0 + t;
+      float l = __shfl_sync(0xffffffffu, l_lane, sidx & 31);
+      if (sidx >= 32 && sidx < n) l = lp[(size_t)(sp.slot_begin + sidx) * n_h + h];
+      const float wgt = (sidx < n && l != -INFINITY) ? expf(l - m) * inv : 0.f;
 #pragma unroll
       for (int v = 0; v < MAXV; ++v) {
-        acc[v].x = fmaf(wgt[t], x[t][v].x, acc[v].x);
-        acc[v].y = fmaf(wgt[t], x[t][v].y, acc[v].y);
-        acc[v].z = fmaf(wgt[t], x[t][v].z, acc[v].z);
-        acc[v].w = fmaf(wgt[t], x[t][v].w, acc[v].w);
+        acc[v].x = fmaf(wgt, x[t][v].x, acc[v].x);
+        acc[v].y = fmaf(wgt, x[t][v].y, acc[v].y);
+        acc[v].z = fmaf(wgt, x[t][v].z, acc[v].z);
+        acc[v].w = fmaf(wgt, x[t][v].w, acc[v].w);
       }
+    }
   }
 #pragma unroll
   for (int v = 0; v < MAXV; ++v) {

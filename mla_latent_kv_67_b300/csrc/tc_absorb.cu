@@ -16,8 +16,9 @@
 //   absorb_out: o[b, h*128 + v] = sum_c o_lat[b, h, c] W^UV[h*128 + v, c]
 //               A = W^UV_h (M = 128, K = 512, K-major), B = o_lat rows. The
 //               fp32 latent output is split into bf16 hi + lo parts (x = hi
-//               + lo to about 16 significant bits) and both are multiplied,
-//               so the tensor-core product keeps fp32-like input precision.
+//               + lo to about 16 significant bits), stacked along N and both
+//               multiplied, so the tensor-core product keeps fp32-like input
+//               precision.
 //
 // Weights come in by TMA with 128-byte swizzle; activations by TMA (q) or
 // by the threads that split them (o_lat). fp32 accumulation in TMEM; one
@@ -65,6 +66,8 @@ __global__ void __launch_bounds__(128)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_q);
     mbar_init(bar_tma, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
@@ -127,12 +130,15 @@ __global__ void __launch_bounds__(128)
 }
 
 // ----------------------------------------------------------- absorb_out
-// smem: A (W^UV_h, 8 chunks of 128 rows x 128 B = 128 KB) | B hi (8 chunks of
-// NT x 128 B) | B lo (same) | barriers.
-constexpr uint32_t AO_A = 0, AO_BHI = 8 * 16384, AO_BLO = AO_BHI + 8 * NT * 128;
-constexpr uint32_t AO_BAR = AO_BLO + 8 * NT * 128;
-constexpr uint32_t AO_SMEM = AO_BAR + 64 + 1024;
-constexpr uint32_t IDESC_AO = idesc_bf16_f32(128, NT, false, false);
+// smem: A (W^UV_h, 8 chunks of 128 rows x 128 B = 128 KB, one barrier per
+// chunk so the products start while later chunks are in flight) | B (8
+// chunks of 2 NT rows x 128 B: rows 0..NT-1 the hi parts of the NT o_lat
+// rows, rows NT..2NT-1 their lo parts) | barriers. One N = 2 NT product per
+// 16-wide K step gives D = [W.hi^T | W.lo^T]; the epilogue adds the halves.
+constexpr int AO_N = 2 * NT;
+constexpr uint32_t AO_A = 0, AO_B = 8 * 16384, AO_BAR = AO_B + 8 * AO_N * 128;
+constexpr uint32_t AO_SMEM = AO_BAR + 128 + 1024;
+constexpr uint32_t IDESC_AO = idesc_bf16_f32(128, AO_N, false, false);
 
 __global__ void __launch_bounds__(128)
     absorb_out_kernel(const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ o_lat,
@@ -140,18 +146,18 @@ __global__ void __launch_bounds__(128)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t bar_tma = sb + AO_BAR, bar_mma = bar_tma + 8;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + AO_BAR + 16);
+  const uint32_t bar_tma = sb + AO_BAR, bar_mma = bar_tma + 8 * 8;  // 8 chunk barriers, then MMA
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + AO_BAR + 80);
   const int h = blockIdx.x, b0 = blockIdx.y * NT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma, 1);
+    tma_prefetch_desc(&tm_w);
+    for (int c = 0; c < 9; ++c) mbar_init(bar_tma + 8 * c, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(tslot), 32);
+    tmem_alloc(smem_u32(tslot), AO_N);
     tmem_relinquish();
     tc_fence_before();
   }
@@ -159,25 +165,38 @@ __global__ void __launch_bounds__(128)
   tc_fence_after();
   const uint32_t tmem = *tslot;
   if (threadIdx.x == 0) {
-    mbar_expect_tx(bar_tma, 8 * 16384);
-    for (int c = 0; c < 8; ++c) tma_load_2d(sb + AO_A + c * 16384, &tm_w, 64 * c, DV * h, bar_tma);
+    for (int c = 0; c < 8; ++c) {
+      mbar_expect_tx(bar_tma + 8 * c, 16384);
+      tma_load_2d(sb + AO_A + c * 16384, &tm_w, 64 * c, DV * h, bar_tma + 8 * c);
+    }
   }
   // B: thread t splits row t / 4, latent chunks 2 (t % 4) and 2 (t % 4) + 1,
-  // into bf16 hi and lo parts, written in the 128-byte-swizzled K-major layout
+  // into bf16 hi (tile row r) and lo (tile row NT + r) parts, written in the
+  // 128-byte-swizzled K-major layout
   {
     const int r = threadIdx.x >> 2, cq = threadIdx.x & 3;
     const bool valid = b0 + r < B;
-    const float4* src = reinterpret_cast<const float4*>(o_lat + ((size_t)(b0 + r) * NH + h) * DC);
+    // rows past the batch read the last row and are zeroed after the loads,
+    // so all 32 loads are unconditional and in flight together
+    const int rb = valid ? b0 + r : B - 1;
+    const float4* src = reinterpret_cast<const float4*>(o_lat + ((size_t)rb * NH + h) * DC);
+    float4 x[2][16];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+      for (int u = 0; u < 16; ++u) x[cc][u] = ld_nc_v4(src + (2 * cq + cc) * 16 + u);
+    if (!valid) {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int u = 0; u < 16; ++u) x[cc][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
       const int c = 2 * cq + cc;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-        if (valid) {
-          x0 = __ldg(src + c * 16 + 2 * u);
-          x1 = __ldg(src + c * 16 + 2 * u + 1);
-        }
+        const float4 x0 = x[cc][2 * u], x1 = x[cc][2 * u + 1];
         const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         uint32_t hi[4], lo[4];
 #pragma unroll
@@ -186,9 +205,12 @@ __global__ void __launch_bounds__(128)
           hi[e] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
           lo[e] = pack_bf16x2(xs[2 * e] - __bfloat162float(h0), xs[2 * e + 1] - __bfloat162float(h1));
         }
-        const uint32_t off = c * NT * 128 + r * 128 + ((u ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(smem + AO_BHI + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(smem + AO_BLO + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        const uint32_t chunk = AO_B + c * AO_N * 128;
+        *reinterpret_cast<uint4*>(smem + chunk + r * 128 + ((u ^ (r & 7)) << 4)) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        const int rl = NT + r;
+        *reinterpret_cast<uint4*>(smem + chunk + rl * 128 + ((u ^ (rl & 7)) << 4)) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
   }
@@ -196,41 +218,42 @@ __global__ void __launch_bounds__(128)
   __syncthreads();
   bool ok = true;
   if (threadIdx.x == 0) {
-    ok = wait_bar(bar_tma, 0, dev_status);
-    if (ok) {
-      tc_fence_after();
 #pragma unroll 1
-      for (int kk = 0; kk < DC / 16; ++kk) {
-        const uint32_t ka = sb + AO_A + (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint32_t kb = (kk >> 2) * NT * 128 + (kk & 3) * 32;
-        mma_ss(tmem, sdesc_sw128(ka, 16, 1024), sdesc_sw128(sb + AO_BHI + kb, 16, 1024), IDESC_AO,
-               kk > 0 ? 1u : 0u);
-        mma_ss(tmem, sdesc_sw128(ka, 16, 1024), sdesc_sw128(sb + AO_BLO + kb, 16, 1024), IDESC_AO, 1u);
-      }
+    for (int c = 0; ok && c < 8; ++c) {
+      ok = wait_bar(bar_tma + 8 * c, 0, dev_status);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tmem, sdesc_sw128(sb + AO_A + c * 16384 + k * 32, 16, 1024),
+               sdesc_sw128(sb + AO_B + c * AO_N * 128 + k * 32, 16, 1024), IDESC_AO,
+               (c > 0 || k > 0) ? 1u : 0u);
     }
-    mma_commit(bar_mma);
+    mma_commit(bar_mma);  // also drains on failure
   }
   ok = __shfl_sync(0xffffffffu, ok, 0);
   const bool done = wait_bar(bar_mma, 0, dev_status);
   if (ok && done) {
     tc_fence_after();
-    uint32_t v[32];
-    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), v);
+    uint32_t vh[32], vl[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), vh);
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + NT, vl);
     tmem_ld_wait();
     const int col = h * DV + 32 * warp + lane;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       if (b0 + j >= B) continue;
+      const float y = __uint_as_float(vh[j]) + __uint_as_float(vl[j]);
       const size_t i = (size_t)(b0 + j) * NH * DV + col;
-      if (out_f32) reinterpret_cast<float*>(o)[i] = __uint_as_float(v[j]);
-      else reinterpret_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16_rn(__uint_as_float(v[j]));
+      if (out_f32) reinterpret_cast<float*>(o)[i] = y;
+      else reinterpret_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16_rn(y);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 32);
+    tmem_dealloc(tmem, AO_N);
   }
 }
 

@@ -79,6 +79,7 @@ class DecodeStep:
         self.u = (torch.empty((B, wl.d_model), dtype=torch.float32, device=dev)
                   if wl.mode == "layer" else None)
         self.max_pages = bt.shape[1]
+        self._side = None  # side stream of run(), made on first use
 
     # ------------------------------------------------------------- stages
     def append(self):
@@ -119,8 +120,20 @@ class DecodeStep:
         return s
 
     def run(self):
+        """One step. The split plan depends only on the lengths, so it runs on
+        a side stream next to the stages before attention (both streams
+        join before the decode kernel; this also captures into a graph)."""
+        main = torch.cuda.current_stream(self.q_cat.device)
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=self.q_cat.device)
+        self._side.wait_stream(main)
+        with torch.cuda.stream(self._side):
+            self.plan()
         for f in self.stages():
-            f()
+            if f.__name__ == "plan":
+                main.wait_stream(self._side)
+            else:
+                f()
 
     def result(self) -> torch.Tensor:
         return self.u if self.wl.mode == "layer" else self.o
