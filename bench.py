@@ -40,6 +40,12 @@ METRIC = "MLA decode μs/step and achieved fraction of roofline (HBM GB/s, TFLOP
 UNIT = "us/step"
 DEFAULT_WORKLOAD = "dsv2_b32_ctx4k"
 
+# DRAM bytes (read + write) of one tcgen05 decode launch, from the ncu
+# capture summarised in profiles/decode_pair_dsv2_b32_ctx4k.md. Valid only
+# for the kernel source that capture measured: set to None whenever the
+# decode kernel changes, until it is captured again.
+DECODE_TRAFFIC = {"dsv2_b32_ctx4k": 157_475_840 + 5_623_296}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -397,7 +403,8 @@ def main():
                    "eager_us_per_step": eager_ms * 1e3,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm" if t_hbm >= t_flop else "tensor", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": DECODE_TRAFFIC.get(wl.name) if path == 1 else None,
                      "kernel": "mla_decode_attn", "kernel_us": attn_ms * 1e3,
                      "alg_bytes": alg_bytes, "alg_flops": alg_flops,
                      "tensor_tflops": tensor_achieved, "tensor_peak": tflops,
