@@ -170,47 +170,50 @@ __global__ void __launch_bounds__(128)
       tma_load_2d(sb + AO_A + c * 16384, &tm_w, 64 * c, DV * h, bar_tma + 8 * c);
     }
   }
-  // B: thread t splits row t / 4, latent chunks 2 (t % 4) and 2 (t % 4) + 1,
-  // into bf16 hi (tile row r) and lo (tile row NT + r) parts, written in the
-  // 128-byte-swizzled K-major layout
+  // B: warp w splits o_lat rows 8w .. 8w + 7 into bf16 hi (tile row r) and
+  // lo (tile row NT + r) parts, written in the 128-byte-swizzled K-major
+  // layout. Lane l holds float4 columns l, l + 32, l + 64, l + 96 of a row,
+  // so each load instruction reads 512 contiguous bytes; all 32 loads of a
+  // thread are in flight together (rows past the batch read the last row and
+  // are zeroed afterwards).
   {
-    const int r = threadIdx.x >> 2, cq = threadIdx.x & 3;
-    const bool valid = b0 + r < B;
-    // rows past the batch read the last row and are zeroed after the loads,
-    // so all 32 loads are unconditional and in flight together
-    const int rb = valid ? b0 + r : B - 1;
-    const float4* src = reinterpret_cast<const float4*>(o_lat + ((size_t)rb * NH + h) * DC);
-    float4 x[2][16];
+    float4 x[8][4];
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc)
+    for (int i = 0; i < 8; ++i) {
+      const int r = 8 * warp + i;
+      const int rb = b0 + r < B ? b0 + r : B - 1;
+      const float4* src = reinterpret_cast<const float4*>(o_lat + ((size_t)rb * NH + h) * DC);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) x[cc][u] = ld_nc_v4(src + (2 * cq + cc) * 16 + u);
-    if (!valid) {
+      for (int q = 0; q < 4; ++q) x[i][q] = ld_nc_v4(src + lane + 32 * q);
+    }
+    if (b0 + 8 * warp + 7 >= B) {  // a tile past the batch's end: zero those rows
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int u = 0; u < 16; ++u) x[cc][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < 4; ++q)
+          if (b0 + 8 * warp + i >= B) x[i][q] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * cq + cc;
+    for (int i = 0; i < 8; ++i) {
+      const int r = 8 * warp + i, rl = NT + r;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float4 x0 = x[cc][2 * u], x1 = x[cc][2 * u + 1];
-        const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        uint32_t hi[4], lo[4];
+      for (int q = 0; q < 4; ++q) {
+        const int f = lane + 32 * q;  // float4 index: columns 4f .. 4f + 3
+        const float4 v = x[i][q];
+        const float xs[4] = {v.x, v.y, v.z, v.w};
+        uint32_t hi[2], lo[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 2; ++e) {
           const __nv_bfloat16 h0 = __float2bfloat16_rn(xs[2 * e]), h1 = __float2bfloat16_rn(xs[2 * e + 1]);
           hi[e] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
           lo[e] = pack_bf16x2(xs[2 * e] - __bfloat162float(h0), xs[2 * e + 1] - __bfloat162float(h1));
         }
-        const uint32_t chunk = AO_B + c * AO_N * 128;
-        *reinterpret_cast<uint4*>(smem + chunk + r * 128 + ((u ^ (r & 7)) << 4)) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        const int rl = NT + r;
-        *reinterpret_cast<uint4*>(smem + chunk + rl * 128 + ((u ^ (rl & 7)) << 4)) =
-            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        // chunk f / 16, 16-byte unit (f % 16) / 2, 8-byte half f % 2
+        const uint32_t chunk = AO_B + (f >> 4) * AO_N * 128, u = (f & 15) >> 1, half = (f & 1) * 8;
+        *reinterpret_cast<uint2*>(smem + chunk + r * 128 + ((u ^ (r & 7)) << 4) + half) =
+            make_uint2(hi[0], hi[1]);
+        *reinterpret_cast<uint2*>(smem + chunk + rl * 128 + ((u ^ (rl & 7)) << 4) + half) =
+            make_uint2(lo[0], lo[1]);
       }
     }
   }
