@@ -82,6 +82,18 @@ def algorithmic(wl, lens):
     return cache + q + o, flops
 
 
+def max_over_ranks(vals, device):
+    """Element-wise max of a list of floats over the ranks of the default
+    process group (the list itself when there is none or only one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 # --------------------------------------------------------------- clocks
 class ClockSampler:
     """Samples SM clock and throttle reasons while the timed loop runs:
@@ -347,10 +359,7 @@ def main():
                 gev[i][1].record(stream)
             barrier()
         step_ms = sum(a.elapsed_time(b) for a, b in gev) / K
-    if world > 1:
-        t = torch.tensor([step_ms, attn_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, attn_ms = t.tolist()
+    step_ms, attn_ms = max_over_ranks([step_ms, attn_ms], dev)
 
     # ---- end to end through the C ABI with host buffers
     q_host = st.q.cpu().pin_memory() if wl.mode == "attn" else st.x.cpu().pin_memory()
@@ -376,10 +385,7 @@ def main():
         if i >= 2:
             e2e.append(a.elapsed_time(b))
     e2e_ms = sum(e2e) / len(e2e)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms, = max_over_ranks([e2e_ms], dev)
     h2d = q_host.numel() * q_host.element_size() + lens_host.numel() * 4 + bt_host.numel() * 4
     d2h = out_host.numel() * out_host.element_size()
 
