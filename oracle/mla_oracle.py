@@ -33,7 +33,7 @@ Conventions: column vectors as in [MLA-V2]; every weight is stored row-major as
 ``W in R^{out x in}``; per-head blocks are consecutive rows (head h owns rows
 ``h*d .. h*d+d-1``).
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
   * one joint latent ``c_KV`` (not separate C_k / C_v);
   * ``k_R`` comes from the token's hidden state through its own matrix W^KR,
     then RoPE; it is not derived from ``c_KV``;
