@@ -15,8 +15,9 @@ of the timed loop; max over ranks. Inputs are resident in HBM. The step's
 calls are recorded once into a CUDA graph and ``value`` times its replays
 (the eager, call-by-call time is reported beside it); the decode kernel's
 own time comes from events around its call in the eager loop. The ``e2e``
-figure times the same step with the per-step inputs copied host->device from
-pinned memory and the result copied back, inside the timed region.
+figure times the same step (the same graph, else the eager calls) with the
+per-step inputs copied host->device from pinned memory before it and the
+result copied back after it, all inside the timed region.
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the path does not shard); there is no collective on the data path.
@@ -378,7 +379,10 @@ def main():
         q_dev.copy_(q_host, non_blocking=True)
         st.seq_lens.copy_(lens_host, non_blocking=True)
         st.block_table.copy_(bt_host, non_blocking=True)
-        st.run()
+        if graph is not None:
+            graph.replay()
+        else:
+            st.run()
         out_host.copy_(res, non_blocking=True)
         b.record(stream)
         b.synchronize()
@@ -406,6 +410,8 @@ def main():
                    "l2": f"flushed before every timed step (read of a {2 * l2 >> 20} MiB buffer, untimed)",
                    "decode_kernel": "tcgen05" if path == 1 else "simt",
                    "step_launch": "cuda_graph" if graph is not None else f"eager ({graph_err})",
+                   "e2e_launch": "pinned copies + cuda_graph + copy back" if graph is not None
+                   else "pinned copies + eager calls + copy back",
                    "eager_us_per_step": eager_ms * 1e3,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm" if t_hbm >= t_flop else "tensor", "achieved": achieved,
