@@ -138,9 +138,12 @@ mla_status mla_absorb_q(const void* q, const void* w_uk, void* q_cat, int B, mla
 
 /* (a4) Split plan. The pages of all sequences, in order, are cut into
  * contiguous ranges of near-equal cost, one per worker (an SM or SM pair of
- * the decode kernel the same dtype/dims select); a sequence cut into k > 1
- * ranges gets k partial results that mla_combine merges. The plan lives in
- * `workspace` and depends only on seq_lens, B, dtype, dims and the device.
+ * the decode kernel the same dtype/dims select). Cost: one unit per page,
+ * plus, on the tcgen05 path, 4 units per sequence a worker starts (its
+ * fixed cost of fetching Q and writing O), so a worker that starts a new
+ * sequence takes fewer pages. A sequence cut into k > 1 ranges gets k
+ * partial results that mla_combine merges. The plan lives in `workspace`
+ * and depends only on seq_lens, B, dtype, dims and the device.
  *   seq_lens [B] int32 (>= 1; tokens already in the cache, including the
  *            one being decoded). */
 size_t mla_decode_workspace_size(int B, mla_dtype dtype, const mla_dims* dims);
