@@ -18,6 +18,7 @@
  *   mla_decode_attn    scores q_cat . [c | k_R], online softmax, latent output
  *   mla_combine        log-sum-exp merge of the split partial results
  *   mla_absorb_out     o_h = W^UV_h o_lat,h                    (per head)
+ *   mla_combine_absorb_out  the two calls above as one
  *   mla_out_proj       u = W^O [o_1; ...; o_n_h]
  *
  * Conventions that hold for every call:
@@ -180,6 +181,17 @@ mla_status mla_combine(const void* workspace, size_t ws_bytes, int B, float* o_l
  *   o     [B][n_h*d_v] in `out_dtype`. fp32 accumulation. */
 mla_status mla_absorb_out(const float* o_lat, const void* w_uv, void* o, int B, mla_dtype dtype,
                           mla_dtype out_dtype, const mla_dims* dims, void* stream);
+
+/* (a6 + a7) mla_combine followed by mla_absorb_out, as one call: the merge
+ * of each split sequence's partials feeds the W^UV product directly. Writes
+ * o_lat and lse exactly as mla_combine does (bit for bit) and o exactly as
+ * mla_absorb_out does. Arguments as for those two calls; `workspace` holds
+ * the plan and partials of the preceding mla_decode_attn. On shapes without
+ * a fused kernel it runs the two kernels one after the other. */
+mla_status mla_combine_absorb_out(const void* workspace, size_t ws_bytes, int B, float* o_lat,
+                                  float* lse, const void* w_uv, void* o, mla_dtype dtype,
+                                  mla_dtype out_dtype, const mla_dims* dims, int32_t* dev_status,
+                                  void* stream);
 
 /* (a8) Output projection u = W^O [o_1; ...; o_n_h] -- DeepSeek-V2 MLA
  * page 2.2 (W^O).

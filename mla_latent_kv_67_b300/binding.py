@@ -58,6 +58,7 @@ _SIGS = {
     "mla_combine": (_I, [_P, _S, _I, _P, _P, _I, _DIMS, _P]),
     "mla_decode_attn_static": (_I, [_P, _P, _P, _I, _I, _P, _I, _F, _P, _P, _I, _DIMS, _P, _P]),
     "mla_absorb_out": (_I, [_P, _P, _P, _I, _I, _I, _DIMS, _P]),
+    "mla_combine_absorb_out": (_I, [_P, _S, _I, _P, _P, _P, _P, _I, _I, _DIMS, _P, _P]),
     "mla_tc_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "mla_out_proj": (_I, [_P, _P, _P, _I, _I, _DIMS, _P]),
 }
@@ -229,6 +230,18 @@ def mla_absorb_out(o_lat, w_uv, o, dims: Dims, stream=None) -> None:
         _ptr(w_uv, shape=(dims.n_h * dims.d_v, dims.d_c), name="w_uv"),
         _ptr(o, shape=(B, dims.n_h * dims.d_v), name="o"), B, _dt(w_uv), _dt(o),
         ctypes.byref(dims), _stream(stream)))
+
+
+def mla_combine_absorb_out(workspace, o_lat, lse, w_uv, o, dims: Dims, dev_status=None,
+                           stream=None) -> None:
+    B = o_lat.shape[0]
+    _check(lib().mla_combine_absorb_out(
+        _ptr(workspace, torch.uint8, name="workspace"), workspace.numel(), B,
+        _ptr(o_lat, torch.float32, (B, dims.n_h, dims.d_c), "o_lat"),
+        _ptr(lse, torch.float32, (B, dims.n_h), "lse"),
+        _ptr(w_uv, shape=(dims.n_h * dims.d_v, dims.d_c), name="w_uv"),
+        _ptr(o, shape=(B, dims.n_h * dims.d_v), name="o"), _dt(w_uv), _dt(o),
+        ctypes.byref(dims), _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
 
 
 def mla_out_proj(o, w_o, u, dims: Dims, stream=None) -> None:

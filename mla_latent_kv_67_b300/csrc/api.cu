@@ -314,6 +314,32 @@ mla_status mla_absorb_out(const float* o_lat, const void* w_uv, void* o, int B, 
   return cuda_status(launch_simt_gemm(g, S(stream)), "absorb_out");
 }
 
+mla_status mla_combine_absorb_out(const void* workspace, size_t ws_bytes, int B, float* o_lat,
+                                  float* lse, const void* w_uv, void* o, mla_dtype dtype,
+                                  mla_dtype out_dtype, const mla_dims* dims, int32_t* dev_status,
+                                  void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  if ((st = check_dtype(out_dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0, "B must be >= 0");
+  if (B == 0) return MLA_OK;
+  REQUIRE(o_lat && lse && w_uv && o, "NULL tensor argument");
+  const int path = pick_path(dtype, dims);
+  const int workers = workers_for(path);
+  if (workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
+  const WorkspaceLayout L = workspace_layout(B, workers, dims->n_h, dims->d_c);
+  if (!workspace || ws_bytes < L.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L.total);
+  if (dtype == MLA_BF16 && g_forced_path != 0 &&
+      tc_absorb_supported(dims->n_h, dims->d_h, dims->d_r, dims->d_c, dims->d_v))
+    return cuda_status(tc_absorb_out_merge_launch(workspace, L, o_lat, lse, w_uv, o,
+                                                  out_dtype == MLA_F32, B, dev_status, S(stream)),
+                       "combine_absorb_out (tcgen05)");
+  if ((st = mla_combine(workspace, ws_bytes, B, o_lat, lse, dtype, dims, stream)) != MLA_OK) return st;
+  return mla_absorb_out(o_lat, w_uv, o, B, dtype, out_dtype, dims, stream);
+}
+
 mla_status mla_out_proj(const void* o, const void* w_o, float* u, int B, mla_dtype dtype,
                         const mla_dims* dims, void* stream) {
   mla_status st = check_dims(dims);

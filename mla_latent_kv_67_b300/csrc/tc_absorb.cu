@@ -260,6 +260,212 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// ------------------------------------------------ combine + absorb_out
+// The split-KV merge (mla_combine) fused into absorb_out: each CTA merges
+// the partial results of its 32 batch rows for its head straight into the
+// B tile, writes the merged o_lat row and lse for the rows the plan split
+// (and zeros / -inf for rows with an invalid length, as mla_combine does),
+// then runs the absorb_out product. Same smem layout and MMA as
+// absorb_out_kernel; 8 warps, each merging 4 rows, two rows at a time with
+// all their loads in flight. The merge is mla_combine's arithmetic in the
+// same order (bitwise the same o_lat and lse).
+constexpr int AM_THREADS = 256;
+
+__global__ void __launch_bounds__(AM_THREADS, 1)
+    absorb_out_merge_kernel(const __grid_constant__ CUtensorMap tm_w, const char* __restrict__ ws,
+                            WorkspaceLayout L, float* __restrict__ o_lat, float* __restrict__ lse,
+                            void* __restrict__ o, int out_f32, int B, int32_t* dev_status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar_tma = sb + AO_BAR, bar_mma = bar_tma + 8 * 8;  // 8 chunk barriers, then MMA
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + AO_BAR + 80);
+  const int h = blockIdx.x, b0 = blockIdx.y * NT;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const SeqPlan* seqs = reinterpret_cast<const SeqPlan*>(ws + L.seqs);
+  const float* lp = reinterpret_cast<const float*>(ws + L.lse_part);
+  const float* op = reinterpret_cast<const float*>(ws + L.o_part);
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_w);
+    for (int c = 0; c < 9; ++c) mbar_init(bar_tma + 8 * c, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tslot), AO_N);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (threadIdx.x == 0) {
+    for (int c = 0; c < 8; ++c) {
+      mbar_expect_tx(bar_tma + 8 * c, 16384);
+      tma_load_2d(sb + AO_A + c * 16384, &tm_w, 64 * c, DV * h, bar_tma + 8 * c);
+    }
+  }
+
+  constexpr int RS = 4;  // splits loaded per round
+#pragma unroll 1
+  for (int pr = 0; pr < 2; ++pr) {
+    // rows ra, ra + 1 of the tile; a row past the batch reads row B - 1
+    // and is dropped
+    int n[2], sbeg[2], bb[2];
+    bool valid[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int r = 4 * warp + 2 * pr + k;
+      valid[k] = b0 + r < B;
+      bb[k] = valid[k] ? b0 + r : B - 1;
+      const SeqPlan sp = seqs[bb[k]];
+      n[k] = valid[k] ? sp.n_splits : 0;
+      sbeg[k] = sp.slot_begin;
+    }
+    // round 0 of both rows: a split past the end re-reads the last one
+    // (weight 0); an unsplit row reads its o_lat row (weight 1)
+    float4 x[2][RS][4];
+    auto src_of = [&](int k, int sidx) -> const float4* {
+      if (n[k] >= 2)
+        return reinterpret_cast<const float4*>(
+            op + ((size_t)(sbeg[k] + min(sidx, n[k] - 1)) * NH + h) * DC);
+      return reinterpret_cast<const float4*>(o_lat + ((size_t)bb[k] * NH + h) * DC);
+    };
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int t = 0; t < RS; ++t) {
+        const float4* src = src_of(k, t);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[k][t][q] = ld_nc_v4(src + lane + 32 * q);
+      }
+    float l_lane[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      l_lane[k] = (n[k] >= 2 && lane < n[k]) ? lp[(size_t)(sbeg[k] + lane) * NH + h] : -INFINITY;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int r = 4 * warp + 2 * pr + k;
+      float4 acc[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      float m = -INFINITY, z = 0.f;
+      if (n[k] == 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = x[k][0][q];
+      } else if (n[k] >= 2) {
+        const int nk = n[k];
+        m = l_lane[k];
+        for (int s0 = 32; s0 < nk; s0 += 32)  // more than 32 splits: rare
+          if (s0 + lane < nk) m = fmaxf(m, lp[(size_t)(sbeg[k] + s0 + lane) * NH + h]);
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
+        z = l_lane[k] == -INFINITY ? 0.f : expf(l_lane[k] - m);
+        for (int s0 = 32; s0 < nk; s0 += 32)
+          if (s0 + lane < nk) {
+            const float l = lp[(size_t)(sbeg[k] + s0 + lane) * NH + h];
+            z += l == -INFINITY ? 0.f : expf(l - m);
+          }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o2);
+        const float inv = 1.f / z;
+        for (int s0 = 0; s0 < nk; s0 += RS) {
+          if (s0 > 0) {  // later rounds (more than RS splits)
+#pragma unroll
+            for (int t = 0; t < RS; ++t) {
+              const float4* src = src_of(k, s0 + t);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) x[k][t][q] = ld_nc_v4(src + lane + 32 * q);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < RS; ++t) {
+            const int sidx = s0 + t;
+            float l = __shfl_sync(0xffffffffu, l_lane[k], sidx & 31);
+            if (sidx >= 32 && sidx < nk) l = lp[(size_t)(sbeg[k] + sidx) * NH + h];
+            const float wgt = (sidx < nk && l != -INFINITY) ? expf(l - m) * inv : 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              acc[q].x = fmaf(wgt, x[k][t][q].x, acc[q].x);
+              acc[q].y = fmaf(wgt, x[k][t][q].y, acc[q].y);
+              acc[q].z = fmaf(wgt, x[k][t][q].z, acc[q].z);
+              acc[q].w = fmaf(wgt, x[k][t][q].w, acc[q].w);
+            }
+          }
+        }
+      }
+      // merged (or invalid-length) rows: o_lat and lse as mla_combine writes them
+      if (valid[k] && n[k] != 1) {
+        float4* orow = reinterpret_cast<float4*>(o_lat + ((size_t)bb[k] * NH + h) * DC);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) orow[lane + 32 * q] = acc[q];
+        if (lane == 0) lse[(size_t)bb[k] * NH + h] = n[k] == 0 ? -INFINITY : m + logf(z);
+      }
+      // hi / lo split into the B tile (rows past the batch are zero)
+      const int rl = NT + r;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = valid[k] ? acc[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float xs[4] = {v.x, v.y, v.z, v.w};
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(xs[2 * e]), h1 = __float2bfloat16_rn(xs[2 * e + 1]);
+          hi[e] = pack_bf16x2(__bfloat162float(h0), __bfloat162float(h1));
+          lo[e] = pack_bf16x2(xs[2 * e] - __bfloat162float(h0), xs[2 * e + 1] - __bfloat162float(h1));
+        }
+        const int f = lane + 32 * q;
+        const uint32_t chunk = AO_B + (f >> 4) * AO_N * 128, u = (f & 15) >> 1, half = (f & 1) * 8;
+        *reinterpret_cast<uint2*>(smem + chunk + r * 128 + ((u ^ (r & 7)) << 4) + half) =
+            make_uint2(hi[0], hi[1]);
+        *reinterpret_cast<uint2*>(smem + chunk + rl * 128 + ((u ^ (rl & 7)) << 4) + half) =
+            make_uint2(lo[0], lo[1]);
+      }
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  bool ok = true;
+  if (threadIdx.x == 0) {
+#pragma unroll 1
+    for (int c = 0; ok && c < 8; ++c) {
+      ok = wait_bar(bar_tma + 8 * c, 0, dev_status);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tmem, sdesc_sw128(sb + AO_A + c * 16384 + k * 32, 16, 1024),
+               sdesc_sw128(sb + AO_B + c * AO_N * 128 + k * 32, 16, 1024), IDESC_AO,
+               (c > 0 || k > 0) ? 1u : 0u);
+    }
+    mma_commit(bar_mma);  // also drains on failure
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  const bool done = wait_bar(bar_mma, 0, dev_status);
+  if (warp < 4 && ok && done) {  // TMEM lanes 32 w .. 32 w + 31: warps 0-3
+    tc_fence_after();
+    uint32_t vh[32], vl[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), vh);
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + NT, vl);
+    tmem_ld_wait();
+    const int col = h * DV + 32 * warp + lane;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      if (b0 + j >= B) continue;
+      const float y = __uint_as_float(vh[j]) + __uint_as_float(vl[j]);
+      const size_t i = (size_t)(b0 + j) * NH * DV + col;
+      if (out_f32) reinterpret_cast<float*>(o)[i] = y;
+      else reinterpret_cast<__nv_bfloat16*>(o)[i] = __float2bfloat16_rn(y);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, AO_N);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -334,6 +540,24 @@ cudaError_t tc_absorb_out_launch(const float* o_lat, const void* w_uv, void* o, 
   if (e != cudaSuccess) return e;
   const dim3 grid(tca::NH, (B + tca::NT - 1) / tca::NT);
   tca::absorb_out_kernel<<<grid, 128, tca::AO_SMEM, s>>>(tm_w, o_lat, o, out_f32, B, dev_status);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_absorb_out_merge_launch(const void* ws, const WorkspaceLayout& L, float* o_lat,
+                                       float* lse, const void* w_uv, void* o, int out_f32, int B,
+                                       int32_t* dev_status, cudaStream_t s) {
+  CUtensorMap tm_w;
+  const cuuint64_t dims[2] = {(cuuint64_t)tca::DC, (cuuint64_t)tca::NH * tca::DV};
+  const cuuint64_t strides[1] = {(cuuint64_t)tca::DC * 2};
+  const cuuint32_t box[2] = {64, 128};
+  cudaError_t e = tca::make_map(&tm_w, w_uv, 2, dims, strides, box);
+  if (e != cudaSuccess) return e;
+  static unsigned long long smem_done = 0;
+  e = set_max_smem_once((const void*)tca::absorb_out_merge_kernel, (int)tca::AO_SMEM, smem_done);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(tca::NH, (B + tca::NT - 1) / tca::NT);
+  tca::absorb_out_merge_kernel<<<grid, tca::AM_THREADS, tca::AO_SMEM, s>>>(
+      tm_w, reinterpret_cast<const char*>(ws), L, o_lat, lse, o, out_f32, B, dev_status);
   return cudaGetLastError();
 }
 

@@ -24,6 +24,10 @@ cudaError_t tc_absorb_q_launch(const void* q, const void* w_uk, void* q_cat, int
                                int32_t* dev_status, cudaStream_t s);
 cudaError_t tc_absorb_out_launch(const float* o_lat, const void* w_uv, void* o, int out_f32, int B,
                                  int32_t* dev_status, cudaStream_t s);
+// mla_combine fused into absorb_out (plan and partials from `ws`).
+cudaError_t tc_absorb_out_merge_launch(const void* ws, const WorkspaceLayout& L, float* o_lat,
+                                       float* lse, const void* w_uv, void* o, int out_f32, int B,
+                                       int32_t* dev_status, cudaStream_t s);
 
 // One page of the decode's tensor-core data path without softmax:
 // s_out[128][64] = q_cat[128][576] . page[64][576]^T and

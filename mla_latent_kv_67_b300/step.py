@@ -80,6 +80,11 @@ class DecodeStep:
                   if wl.mode == "layer" else None)
         self.max_pages = bt.shape[1]
         self._side = None  # side stream of run(), made on first use
+        # mla_combine_absorb_out instead of the two calls: bit-identical, but
+        # measured slower on B300 (dsv2_b32_ctx4k step 80 vs 79 us) -- the
+        # merge inside the W^UV kernel serialises partial loads that the
+        # separate merge kernel spreads over all SMs. Off by default.
+        self.fuse_out = False
 
     # ------------------------------------------------------------- stages
     def append(self):
@@ -107,6 +112,10 @@ class DecodeStep:
     def absorb_out(self):
         M.mla_absorb_out(self.o_lat, self.w_uv, self.o, self.dims)
 
+    def combine_absorb_out(self):
+        M.mla_combine_absorb_out(self.workspace, self.o_lat, self.lse, self.w_uv, self.o, self.dims,
+                                 self.dev_status)
+
     def out_proj(self):
         M.mla_out_proj(self.o, self.w_o, self.u, self.dims)
 
@@ -114,7 +123,11 @@ class DecodeStep:
         s = []
         if self.wl.mode in ("layer", "prefill"):
             s += [self.append, self.project]
-        s += [self.absorb_q, self.plan, self.attend, self.combine, self.absorb_out]
+        s += [self.absorb_q, self.plan, self.attend]
+        if self.fuse_out:
+            s.append(self.combine_absorb_out)
+        else:
+            s += [self.combine, self.absorb_out]
         if self.wl.mode == "layer":
             s.append(self.out_proj)
         return s
