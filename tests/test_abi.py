@@ -85,3 +85,23 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(M.MlaError):
         M.mla_absorb_q(q, torch.zeros(8, 32, dtype=torch.bfloat16),
                        torch.zeros(1, 2, 34, dtype=torch.bfloat16), d)
+
+
+def declared_arity():
+    """Parameter count of every function the header declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(mla_\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """Every entry the Python binding types has the header's parameter
+    count, so a changed C signature cannot silently shift arguments."""
+    arity = declared_arity()
+    for name, (_, args) in M._SIGS.items():
+        assert name in arity, f"{name} is typed in the binding but not declared"
+        assert len(args) == arity[name], f"{name}: binding {len(args)} args, header {arity[name]}"
