@@ -105,3 +105,19 @@ def test_binding_signatures_match_the_header():
     for name, (_, args) in M._SIGS.items():
         assert name in arity, f"{name} is typed in the binding but not declared"
         assert len(args) == arity[name], f"{name}: binding {len(args)} args, header {arity[name]}"
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_is_plain_c(tmp_path, lang, std):
+    """The boundary header compiles as strict C99 and as C++ (no CUDA, torch
+    or C++-only types in any signature)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip(f"no {lang} compiler")
+    src = tmp_path / "use.c"
+    src.write_text('#include "mla_b300.h"\nint main(void) { return (int)mla_abi_version(); }\n')
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-x", lang,
+                        "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
