@@ -121,3 +121,30 @@ def test_header_is_plain_c(tmp_path, lang, std):
     r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-x", lang,
                         "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_c_program_links_and_runs_host_calls(tmp_path):
+    """A plain C program links against the library and calls it through the
+    ABI alone (host-only calls, so no GPU is needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(M.LIB_PATH)
+    src = tmp_path / "prog.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <string.h>\n#include "mla_b300.h"\n'
+        'int main(void) {\n'
+        '  if (mla_abi_version() != 1) return 1;\n'
+        '  if (strcmp(mla_status_string(MLA_OK), "MLA_OK") != 0) return 2;\n'
+        '  mla_dims d = {128, 128, 64, 512, 128, 0, 0, 64};\n'
+        '  if (mla_absorb_q(NULL, NULL, NULL, 4, MLA_BF16, &d, NULL) != MLA_ERR_INVALID_ARG) return 3;\n'
+        '  printf("ok %s\\n", mla_last_error());\n  return 0;\n}\n')
+    exe = tmp_path / "prog"
+    r = subprocess.run([cc, "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                        "-L", libdir, "-lmla_b300", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), (r.returncode, r.stdout, r.stderr)
