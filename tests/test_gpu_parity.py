@@ -153,6 +153,21 @@ def test_device_status_reports_bad_block_and_length():
     assert torch.all(st.o_lat[2] == 0) and torch.all(torch.isinf(st.lse[2]))
 
 
+def test_bf16_sequence_split_over_32_ways():
+    """One 131072-token sequence among fifteen short ones: the plan splits it
+    over more than 32 workers, so the merge takes its second pass over the
+    split lse values; that sequence and a short one against the oracle."""
+    wl = RAGGED.replace(name="many_splits", batch=16, shuffle_pages=True,
+                        lens=tuple([131072] + [700 + 37 * i for i in range(15)]))
+    st = run(wl)
+    if M.mla_decode_path(st.dtype, st.dims) == 1:
+        seq0 = st.workspace[256:256 + 32].cpu().numpy().view(np.int32)  # SeqPlan of sequence 0
+        assert seq0[3] > 32, f"only {seq0[3]} splits"
+    ex = Expected(wl)
+    for b in (0, 7):
+        check_seq(st, ex, b, TOL_BF16, explicit_heads=[33])
+
+
 # ---------------------------------------------------- full-size workloads
 def _sampled(name, seqs, explicit_heads, what=("o_lat", "o", "lse")):
     wl = synth.WORKLOADS[name]
