@@ -4,7 +4,9 @@
 A step is one pass of the decode path over one batch of synthetic input
 (default workload: DeepSeek-V2 shapes, batch 32, 4096-token contexts, bf16
 paged cache): absorb_q -> plan -> decode_attn -> combine -> absorb_out, all
-through the C ABI. ``--workload`` picks another of the five workloads.
+through the C ABI. ``--workload`` picks another of the five workloads; the
+line also carries ``other_workloads``: the long-context, ragged and
+full-layer workloads measured the same way, each with its own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -13,11 +15,16 @@ Timing: W untimed warm-up steps, then K steps, each preceded by an L2 flush
 with CUDA events on the launching stream; barrier + synchronize on both sides
 of the timed loop; max over ranks. Inputs are resident in HBM. The step's
 calls are recorded once into a CUDA graph and ``value`` times its replays
-(the eager, call-by-call time is reported beside it); the decode kernel's
-own time comes from events around its call in the eager loop. The ``e2e``
-figure times the same step (the same graph, else the eager calls) with the
+(the eager, call-by-call time is reported beside it). Each stage is also
+recorded into a graph of its own and timed alone after a flush: the decode
+kernel's duration (``roofline.kernel_us``) comes from that, so host launch
+overhead never enters it. The ``e2e`` figure times the same step with the
 per-step inputs copied host->device from pinned memory before it and the
-result copied back after it, all inside the timed region.
+result copied back after it, all inside the timed region, and splits the
+time into those three parts.
+
+``--impl reference`` times the fp64 explicit oracle on the host cores, each
+step one whole oracle step of the workload (every sequence and head).
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the path does not shard); there is no collective on the data path.
@@ -41,10 +48,10 @@ METRIC = "MLA decode μs/step and achieved fraction of roofline (HBM GB/s, TFLOP
 UNIT = "us/step"
 DEFAULT_WORKLOAD = "dsv2_b32_ctx4k"
 
-# DRAM bytes (read + write) of one tcgen05 decode launch, from the ncu
-# capture summarised in profiles/decode_pair_dsv2_b32_ctx4k.md. Valid only
-# for the kernel source that capture measured: set to None whenever the
-# decode kernel changes, until it is captured again.
+# DRAM bytes (read + write) of one tcgen05 decode launch, from an ncu
+# capture of that kernel on the workload. Valid only for the kernel source
+# the capture measured: drop the entry whenever the decode kernel changes,
+# until it is captured again.
 DECODE_TRAFFIC = {"dsv2_b32_ctx4k": 157_475_840 + 5_623_296}
 
 
@@ -56,8 +63,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0,
-                    help="target CPU time of the oracle sample")
+    ap.add_argument("--no-other", action="store_true",
+                    help="measure only --workload (skip the other_workloads entries)")
     return ap.parse_args()
 
 
@@ -179,33 +186,45 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------- CPU oracle
-def cpu_oracle_sample(wl, target_s: float, seqs_heads=None):
-    """Time the fp64 explicit oracle on a bounded sample of the workload:
-    (sequence, head) pairs in a fixed order until ``target_s`` seconds have
-    been spent. Returns (seconds, pairs done, token-heads done)."""
+def oracle_step(wl):
+    """One whole step of the fp64 explicit oracle on this host's cores: for
+    every sequence, its cached rows (drawn, plus the rows the append step
+    writes on the full-layer and prefill workloads), its query (drawn, or
+    projected from the token), then every head rebuilt as
+    K_h = [c W^UK_h^T | k_R], V_h = c W^UV_h^T and attended with plain
+    softmax, and W^O on the full-layer workload. Returns the seconds spent
+    inside the oracle (drawing the seeded inputs is outside the clock)."""
     from oracle import mla_oracle as O
     from mla_latent_kv_67_b300 import synth
     lens = synth.seq_lens(wl)
-    w_uk = synth.weight(wl, "w_uk").astype(np.float64)
-    w_uv = synth.weight(wl, "w_uv").astype(np.float64)
-    q = synth.query(wl).astype(np.float64)
-    # heads in a spread order (0, 16, 32, ..., 1, 17, ...), sequences inner
-    order = [h0 + k for h0 in range(16) for k in range(0, wl.n_h, 16) if h0 + k < wl.n_h]
-    pairs = seqs_heads or [(b, h) for h in order for b in range(wl.batch)]
-    spent, done, tok, rows_cache = 0.0, 0, 0, {}
-    for b, h in pairs:
-        if b not in rows_cache:
-            rows_cache = {b: synth.cache_rows(wl, b, int(lens[b])).astype(np.float64)}
-        rows = rows_cache[b]
+    w = {k: synth.weight(wl, k).astype(np.float64) for k in ("w_uk", "w_uv")}
+    if wl.mode == "attn":
+        q = synth.query(wl).astype(np.float64)
+    else:
+        for k in ("w_dkv", "w_kr", "w_uq", "w_qr") + (("w_dq",) if wl.d_cq else ()) + \
+                (("w_o",) if wl.mode == "layer" else ()):
+            w[k] = synth.weight(wl, k).astype(np.float64)
+        x = synth.tokens(wl).astype(np.float64)
+    drawn = synth.drawn_rows(wl, lens)
+    spent = 0.0
+    for b in range(wl.batch):
+        rows = synth.cache_rows(wl, b, int(drawn[b])).astype(np.float64)
         t = time.perf_counter()
-        O.attention_explicit(q[b, :, :wl.d_h], q[b, :, wl.d_h:], rows[:, :wl.d_c], rows[:, wl.d_c:],
-                             w_uk, w_uv, wl.scale, heads=[h])
+        c, k = rows[:, :wl.d_c], rows[:, wl.d_c:]
+        if wl.mode == "attn":
+            q_c, q_r = q[b, :, :wl.d_h], q[b, :, wl.d_h:]
+        else:
+            xs = x[b:b + 1] if wl.mode == "layer" else x
+            pos = np.arange(int(drawn[b]), int(lens[b]))
+            c2, k2 = O.latent_cache_row(xs, w["w_dkv"], w["w_kr"], pos, wl.rope_base)
+            c, k = np.concatenate([c, c2]), np.concatenate([k, k2])
+            q_c, q_r = O.project_query(xs[-1], w["w_uq"], w["w_qr"], int(lens[b]) - 1, wl.n_h,
+                                       w_dq=w.get("w_dq"), base=wl.rope_base)
+        o, _ = O.attention_explicit(q_c, q_r, c, k, w["w_uk"], w["w_uv"], wl.scale)
+        if wl.mode == "layer":
+            O.output_projection(o, w["w_o"])
         spent += time.perf_counter() - t
-        done += 1
-        tok += int(lens[b])
-        if spent >= target_s:
-            break
-    return spent, done, tok
+    return spent
 
 
 def blas_threads():
@@ -216,18 +235,16 @@ def blas_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline_entry(wl, target_s):
-    """The oracle timed on this host's cores on a bounded sample, extrapolated
-    by token-heads to one full step."""
-    from mla_latent_kv_67_b300 import synth
-    lens = synth.seq_lens(wl)
-    spent, pairs, tok = cpu_oracle_sample(wl, target_s)
-    full = float(np.sum(lens)) * wl.n_h
-    us = spent * full / tok * 1e6
-    return {"value": us, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": f"fp64 explicit (non-absorbed) oracle on {pairs} of {wl.batch * wl.n_h} "
-                      f"(sequence, head) pairs ({spent:.1f} s), extrapolated by token-heads "
-                      f"to the full step"}
+def oracle_sample_text(wl):
+    return (f"one whole step: the fp64 explicit (non-absorbed) oracle over all "
+            f"{wl.batch} x {wl.n_h} (sequence, head) pairs of {wl.name}")
+
+
+def cpu_baseline_entry(wl):
+    """The oracle timed on this host's cores over one whole step."""
+    spent = oracle_step(wl)
+    return {"value": spent * 1e6, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": oracle_sample_text(wl)}
 
 
 # -------------------------------------------------------------- reference
@@ -238,15 +255,13 @@ def run_reference(args):
     from mla_latent_kv_67_b300 import synth
     wl = synth.WORKLOADS[args.workload]
     lens = synth.seq_lens(wl)
-    # each step: one (sequence, head) pair of the explicit oracle, rotating
-    pairs = [(b, h) for h in range(wl.n_h) for b in range(wl.batch)]
-    spent_t, tok_t = 0.0, 0
+    t_run = time.perf_counter()
+    times = []
     for i in range(args.warmup + args.steps):
-        b, h = pairs[i % len(pairs)]
-        spent, _, tok = cpu_oracle_sample(wl, 0.0, seqs_heads=[(b, h)])
+        spent = oracle_step(wl)
         if i >= args.warmup:
-            spent_t, tok_t = spent_t + spent, tok_t + tok
-    us = spent_t / tok_t * float(np.sum(lens)) * wl.n_h * 1e6
+            times.append(spent)
+    us = sum(times) / len(times) * 1e6
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -254,14 +269,116 @@ def run_reference(args):
                                             "ctx": int(lens.max()), "n_h": wl.n_h, "d_c": wl.d_c,
                                             "d_r": wl.d_r, "page_size": wl.page_size},
             "cpu_baseline": {"value": us, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                             "sample": f"each step: the fp64 explicit oracle on one (sequence, head) "
-                                       f"pair, extrapolated by token-heads to the full step"},
-            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                             "sample": oracle_sample_text(wl)},
+            "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": time.perf_counter() - t_run}
     print(json.dumps(line), flush=True)
     return 0
 
 
 # -------------------------------------------------------------------- ours
+def weight_bytes(wl):
+    """Bytes of the weights one step of the workload reads (bf16 or fp32)."""
+    esz = 2 if wl.dtype == "bf16" else 4
+    n = wl.n_h * wl.d_h * wl.d_c + wl.n_h * wl.d_v * wl.d_c     # W^UK, W^UV
+    if wl.mode == "layer":
+        k = wl.d_cq or wl.d_model
+        n += (wl.d_c + wl.d_r) * wl.d_model                      # W^DKV | W^KR
+        n += wl.d_cq * wl.d_model                                # W^DQ
+        n += wl.n_h * (wl.d_h + wl.d_r) * k                      # W^UQ | W^QR
+        n += wl.d_model * wl.n_h * wl.d_v                        # W^O
+    return n * esz, n
+
+
+def step_roofline(wl, lens, hbm, tflops, step_us):
+    """Roofline of the whole step: the decode launch's algorithmic bytes and
+    FLOPs plus every weight read once and its product with the batch."""
+    b, f = algorithmic(wl, lens)
+    wb, wn = weight_bytes(wl)
+    b += wb
+    f += 2 * wl.batch * wn
+    t = max(b / (hbm * 1e9), f / (tflops * 1e12))
+    return {"alg_bytes": b, "alg_flops": f, "roofline_us": t * 1e6,
+            "frac": t * 1e6 / step_us if step_us else None}
+
+
+def time_graph(g, K, flush, stream):
+    """Mean CUDA-event time (ms) of K replays of graph g, L2 flushed before each."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / K
+
+
+def capture(fn):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        fn()
+    return g
+
+
+def measure_workload(wl, dev, K, W, flush, stream, hbm, tflops, barrier=None, sampler=None):
+    """Step and per-stage times of one workload: the step as one CUDA graph
+    (value), each stage as a graph of its own timed alone, the decode
+    kernel's roofline."""
+    import torch
+    from mla_latent_kv_67_b300 import binding as M
+    from mla_latent_kv_67_b300.step import DecodeStep
+    st = DecodeStep(wl, device=dev)
+    for _ in range(W):
+        flush()
+        st.run()
+    torch.cuda.synchronize()
+    assert st.status() == 0, f"{wl.name}: device status {st.status():#x}"
+    g = capture(st.run)
+    for _ in range(W):
+        flush()
+        g.replay()
+    torch.cuda.synchronize()
+    assert st.status() == 0, f"{wl.name}: device status {st.status():#x}"
+    if barrier:
+        barrier()
+    if sampler is not None:
+        with sampler:
+            step_ms = time_graph(g, K, flush, stream)
+    else:
+        step_ms = time_graph(g, K, flush, stream)
+    stages = {}
+    for f in st.stages():
+        gs = capture(f)
+        for _ in range(2):
+            flush()
+            gs.replay()
+        stages[f.__name__] = time_graph(gs, K, flush, stream) * 1e3
+    torch.cuda.synchronize()
+    assert st.status() == 0, f"{wl.name}: device status {st.status():#x}"
+    kernel_us = stages["attend"]
+    alg_bytes, alg_flops = algorithmic(wl, st.lens_np)
+    t_hbm = alg_bytes / (hbm * 1e9)
+    t_flop = alg_flops / (tflops * 1e12)
+    achieved = alg_bytes / (kernel_us * 1e-6) / 1e9
+    tensor = alg_flops / (kernel_us * 1e-6) / 1e12
+    path = M.mla_decode_path(st.dtype, st.dims)
+    roof = {"bound": "hbm" if t_hbm >= t_flop else "tensor", "achieved": achieved, "peak": hbm,
+            "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": DECODE_TRAFFIC.get(wl.name) if path == 1 else None,
+            "kernel": "mla_decode_attn", "kernel_us": kernel_us,
+            "alg_bytes": alg_bytes, "alg_flops": alg_flops,
+            "tensor_tflops": tensor, "tensor_peak": tflops, "tensor_frac": tensor / tflops,
+            "roofline_us": max(t_hbm, t_flop) * 1e6,
+            "frac_of_roofline": max(t_hbm, t_flop) * 1e6 / kernel_us}
+    return st, g, {"step_us": step_ms * 1e3, "stages_us": stages, "roofline": roof,
+                   "decode_kernel": "tcgen05" if path == 1 else "simt",
+                   "step_roofline": step_roofline(wl, st.lens_np, hbm, tflops, step_ms * 1e3)}
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -278,128 +395,86 @@ def main():
 
     from mla_latent_kv_67_b300 import build as mbuild
     mbuild.build()
-    from mla_latent_kv_67_b300 import binding as M
     from mla_latent_kv_67_b300 import synth
-    from mla_latent_kv_67_b300.step import DecodeStep
 
     wl = synth.WORKLOADS[args.workload]
-    st = DecodeStep(wl, device=dev)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
 
-    def do_flush():
-        flush.sum()
-
-    tc = M.mla_decode_path(st.dtype, st.dims) == 1
-    launches_per_step = 0
-    for f in st.stages():
-        launches_per_step += {"absorb_q": 1 if tc else 2,
-                              "project": 2 if wl.d_cq else 1}.get(f.__name__, 1)
+    def flush():
+        flush_buf.sum()
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        do_flush()
-        st.run()
-    barrier()
-    assert st.status() == 0, f"device status {st.status():#x}"
-
-    # The step's calls recorded once into a CUDA graph (the library allocates
-    # nothing and only enqueues work, so the calls capture as they are).
-    graph, graph_err = None, None
-    try:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, capture_error_mode="relaxed"):
-            st.run()
-        for _ in range(args.warmup):
-            do_flush()
-            g.replay()
-        barrier()
-        assert st.status() == 0, f"device status {st.status():#x}"
-        graph = g
-    except Exception as e:  # noqa: BLE001
-        graph_err = f"{type(e).__name__}: {e}"[:200]
-
+    hbm, tflops, peak_kind = peaks()
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    ka = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(local)
+    st, graph, res = measure_workload(wl, dev, K, args.warmup, flush, stream, hbm, tflops,
+                                      barrier=barrier, sampler=sampler)
     stages = st.stages()
-    with sampler:
-        barrier()
-        t_wall = time.perf_counter()
-        for i in range(K):
-            do_flush()
-            ev[i][0].record(stream)
-            for f in stages:
-                if f.__name__ == "attend":
-                    ka[i][0].record(stream)
-                    f()
-                    ka[i][1].record(stream)
-                else:
-                    f()
-            ev[i][1].record(stream)
-        barrier()
-        t_wall = time.perf_counter() - t_wall
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    attn_ms = sum(a.elapsed_time(b) for a, b in ka) / K
-    eager_ms = step_ms
-    if graph is not None:
-        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-        with sampler:
-            barrier()
-            for i in range(K):
-                do_flush()
-                gev[i][0].record(stream)
-                graph.replay()
-                gev[i][1].record(stream)
-            barrier()
-        step_ms = sum(a.elapsed_time(b) for a, b in gev) / K
-    step_ms, attn_ms = max_over_ranks([step_ms, attn_ms], dev)
 
-    # ---- end to end through the C ABI with host buffers
+    # the same step, call by call (eager), for comparison
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    barrier()
+    for i in range(K):
+        flush()
+        ev[i][0].record(stream)
+        st.run()
+        ev[i][1].record(stream)
+    barrier()
+    eager_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    step_ms = res["step_us"] / 1e3
+    kernel_ms = res["roofline"]["kernel_us"] / 1e3
+    step_ms, kernel_ms, eager_ms = max_over_ranks([step_ms, kernel_ms, eager_ms], dev)
+
+    # ---- end to end with host buffers: pinned H2D of the step's inputs, the
+    # step's graph, D2H of its result, all inside the timed region
     q_host = st.q.cpu().pin_memory() if wl.mode == "attn" else st.x.cpu().pin_memory()
     q_dev = st.q if wl.mode == "attn" else st.x
     lens_host = st.seq_lens.cpu().pin_memory()
     bt_host = st.block_table.cpu().pin_memory()
-    res = st.result()
-    out_host = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
+    out = st.result()
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     Ke = min(K, 100)
-    e2e = []
+    parts = []
     for i in range(Ke + 2):
-        do_flush()
+        flush()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
         q_dev.copy_(q_host, non_blocking=True)
         st.seq_lens.copy_(lens_host, non_blocking=True)
         st.block_table.copy_(bt_host, non_blocking=True)
-        if graph is not None:
-            graph.replay()
-        else:
-            st.run()
-        out_host.copy_(res, non_blocking=True)
-        b.record(stream)
-        b.synchronize()
+        e[1].record(stream)
+        graph.replay()
+        e[2].record(stream)
+        out_host.copy_(out, non_blocking=True)
+        e[3].record(stream)
+        e[3].synchronize()
         if i >= 2:
-            e2e.append(a.elapsed_time(b))
-    e2e_ms = sum(e2e) / len(e2e)
+            parts.append([e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]),
+                          e[2].elapsed_time(e[3]), e[0].elapsed_time(e[3])])
+    h2d_ms, mid_ms, d2h_ms, e2e_ms = (sum(p[j] for p in parts) / len(parts) for j in range(4))
     e2e_ms, = max_over_ranks([e2e_ms], dev)
     h2d = q_host.numel() * q_host.element_size() + lens_host.numel() * 4 + bt_host.numel() * 4
     d2h = out_host.numel() * out_host.element_size()
 
-    hbm, tflops, peak_kind = peaks()
-    alg_bytes, alg_flops = algorithmic(wl, st.lens_np)
-    achieved = alg_bytes / (attn_ms * 1e-3) / 1e9
-    tensor_achieved = alg_flops / (attn_ms * 1e-3) / 1e12
-    t_hbm = alg_bytes / (hbm * 1e9)
-    t_flop = alg_flops / (tflops * 1e12)
-    path = M.mla_decode_path(st.dtype, st.dims)
+    roof = dict(res["roofline"])
+    roof["kernel_us"] = kernel_ms * 1e3
+    roof["achieved"] = roof["alg_bytes"] / (kernel_ms * 1e-3) / 1e9
+    roof["frac"] = roof["achieved"] / hbm
+    roof["tensor_tflops"] = roof["alg_flops"] / (kernel_ms * 1e-3) / 1e12
+    roof["tensor_frac"] = roof["tensor_tflops"] / tflops
+    roof["frac_of_roofline"] = roof["roofline_us"] / (kernel_ms * 1e3)
+    roof["peak_source"] = peak_kind
+    roof["timing"] = "decode launch alone in its own CUDA graph, L2 flushed before each"
+    launches = sum({"absorb_q": 1 if res["decode_kernel"] == "tcgen05" else 2,
+                    "project": 2 if wl.d_cq else 1}.get(f.__name__, 1) for f in stages)
     line = {
         "metric": METRIC, "value": step_ms * 1e3, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False,
@@ -408,35 +483,48 @@ def main():
                    "ctx_total": int(st.lens_np.sum()), "n_h": wl.n_h, "d_c": wl.d_c,
                    "d_r": wl.d_r, "page_size": wl.page_size,
                    "l2": f"flushed before every timed step (read of a {2 * l2 >> 20} MiB buffer, untimed)",
-                   "decode_kernel": "tcgen05" if path == 1 else "simt",
-                   "step_launch": "cuda_graph" if graph is not None else f"eager ({graph_err})",
-                   "e2e_launch": "pinned copies + cuda_graph + copy back" if graph is not None
-                   else "pinned copies + eager calls + copy back",
+                   "decode_kernel": res["decode_kernel"], "step_launch": "cuda_graph",
+                   "e2e_launch": "pinned copies + cuda_graph + copy back",
                    "eager_us_per_step": eager_ms * 1e3,
+                   "stages_us": res["stages_us"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm" if t_hbm >= t_flop else "tensor", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": DECODE_TRAFFIC.get(wl.name) if path == 1 else None,
-                     "kernel": "mla_decode_attn", "kernel_us": attn_ms * 1e3,
-                     "alg_bytes": alg_bytes, "alg_flops": alg_flops,
-                     "tensor_tflops": tensor_achieved, "tensor_peak": tflops,
-                     "tensor_frac": tensor_achieved / tflops,
-                     "roofline_us": max(t_hbm, t_flop) * 1e6,
-                     "frac_of_roofline": max(t_hbm, t_flop) / (attn_ms * 1e-3),
-                     "peak_source": peak_kind},
+        "roofline": roof,
+        "step_roofline": res["step_roofline"],
         "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * K * (2 if graph is not None else 1),
+                "d2h_bytes_per_step": d2h, "h2d_us": h2d_ms * 1e3, "step_us": mid_ms * 1e3,
+                "d2h_us": d2h_ms * 1e3},
+        "gpu_launches": launches * K,
         "clocks": sampler.summary(),
-        "wall_s_timed": t_wall,
     }
+    del st, graph
+    torch.cuda.empty_cache()
+    if not args.no_other and world == 1:
+        others = {}
+        for name in OTHER_WORKLOADS:
+            if name == wl.name:
+                continue
+            ow = synth.WORKLOADS[name]
+            ost, og, ores = measure_workload(ow, dev, max(3, min(K, 20)), max(3, min(args.warmup, 5)),
+                                             flush, stream, hbm, tflops)
+            ores["roofline"]["peak_source"] = peak_kind
+            ores["config"] = {"batch": ow.batch, "ctx_total": int(ost.lens_np.sum()),
+                              "ctx_max": int(ost.lens_np.max()), "mode": ow.mode}
+            others[name] = ores
+            del ost, og
+            torch.cuda.empty_cache()
+        line["other_workloads"] = others
     if rank == 0 and world == 1 and not args.no_cpu_baseline and wl.mode == "attn":
-        line["cpu_baseline"] = cpu_baseline_entry(wl, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline_entry(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+# measured beside the headline workload in the same run (the tiny fp32
+# workload is a parity case only)
+OTHER_WORKLOADS = ("dsv2_b4_ctx128k", "dsv2_b128_ragged", "dsv2_layer_b64_ctx32k")
 
 
 if __name__ == "__main__":

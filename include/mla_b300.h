@@ -202,17 +202,16 @@ mla_status mla_out_proj(const void* o, const void* w_o, float* u, int B, mla_dty
 
 /* Allocation-free decode (the paper has no counterpart: this is a service
  * for callers, not a step of the method). Some callers cannot allocate
- * device memory when they decode -- code under a CUDA stream capture in
- * global mode, where cudaMalloc is refused; plugin hosts and embedded
- * runtimes that hand over a stream but no allocator; serving loops that ban
- * driver allocations after start-up so no step blocks on the allocator --
- * and so cannot supply the workspace mla_decode_attn needs. This call runs
- * the same plan -> decode -> combine sequence with that workspace held in a
+ * device memory when they decode -- plugin hosts and embedded runtimes that
+ * hand over a stream but no allocator; serving loops that ban device
+ * allocations after start-up so no step blocks on the allocator -- and so
+ * cannot supply the workspace mla_decode_attn needs. This call runs the same
+ * plan -> decode -> combine sequence with that workspace held in a
  * file-scope device array of MLA_STATIC_SCRATCH_BYTES, which every GPU that
  * loads this library keeps until the process exits. It calls no cudaMalloc,
  * cudaFree or allocating library routine.
- *   Arguments and outputs are those of mla_decode_attn (o_lat and lse are
- *   final for every sequence; no mla_combine call follows).
+ *   Arguments, checks and outputs are those of mla_decode_attn (o_lat and
+ *   lse are final for every sequence; no mla_combine call follows).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.

@@ -14,6 +14,7 @@ using namespace mla;
 namespace {
 
 thread_local std::string g_last_error;
+int g_forced_path = -1;
 
 mla_status fail(mla_status st, const char* fmt, ...) {
   char buf[512];
@@ -35,6 +36,14 @@ mla_status cuda_status(cudaError_t e, const char* what) {
     if (!(cond)) return fail(MLA_ERR_INVALID_ARG, __VA_ARGS__); \
   } while (0)
 
+cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+namespace mla {
+// Records `msg` as this host thread's mla_last_error() and returns `st`.
+mla_status record_error(mla_status st, const char* msg) { return fail(st, "%s", msg); }
+
 mla_status check_dims(const mla_dims* d) {
   REQUIRE(d != nullptr, "dims is NULL");
   REQUIRE(d->n_h > 0 && d->d_h > 0 && d->d_c > 0 && d->d_v > 0 && d->page_size > 0,
@@ -50,7 +59,6 @@ mla_status check_dtype(int dt) {
   return MLA_OK;
 }
 
-int g_forced_path = -1;
 
 int device_sms() {
   int dev = 0, sms = 0;
@@ -71,13 +79,39 @@ int workers_for(int path) {
   return path == 1 ? tc_pair_workers(sms) : sms;
 }
 
-cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-}  // namespace
+cudaError_t launch_decode(const DecodeSetup& ds, const void* q_cat, const void* cache,
+                          const int32_t* block_table, int max_pages, int num_pages, int B,
+                          float softmax_scale, void* ws, float* o_lat, float* lse, mla_dtype dtype,
+                          const mla_dims* d, int32_t* dev_status, cudaStream_t s) {
+  if (ds.path == 1)
+    return tc_pair_launch(q_cat, cache, block_table, max_pages, num_pages, B, ds.workers,
+                          softmax_scale, ws, ds.L, o_lat, lse, dev_status, s);
+  return launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, B, ds.workers,
+                            softmax_scale, ws, ds.L, o_lat, lse, d->n_h, d->d_c, d->d_r,
+                            d->page_size, dtype == MLA_F32, dev_status, s);
+}
 
-namespace mla {
-// Records `msg` as this host thread's mla_last_error() and returns `st`.
-mla_status record_error(mla_status st, const char* msg) { return fail(st, "%s", msg); }
+mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* block_table,
+                        int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                        const float* o_lat, const float* lse, mla_dtype dtype,
+                        const mla_dims* dims, DecodeSetup* out) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0, "B must be >= 0");
+  out->path = 0;
+  out->workers = 0;
+  if (B == 0) return MLA_OK;
+  REQUIRE(q_cat && cache && block_table && seq_lens && o_lat && lse, "NULL tensor argument");
+  REQUIRE(max_pages > 0 && num_pages > 0, "max_pages and num_pages must be > 0");
+  REQUIRE(dims->d_c % 32 == 0 && dims->d_c <= 512, "d_c must be a multiple of 32, <= 512");
+  out->path = pick_path(dtype, dims);
+  out->workers = workers_for(out->path);
+  if (out->workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
+  out->L = workspace_layout(B, out->workers, dims->n_h, dims->d_c);
+  return MLA_OK;
+}
 }  // namespace mla
 
 extern "C" {
@@ -246,31 +280,17 @@ mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* 
                            float softmax_scale, void* workspace, size_t ws_bytes, float* o_lat,
                            float* lse, mla_dtype dtype, const mla_dims* dims,
                            int32_t* dev_status, void* stream) {
-  mla_status st = check_dims(dims);
-  if (st != MLA_OK) return st;
-  if ((st = check_dtype(dtype)) != MLA_OK) return st;
-  REQUIRE(B >= 0, "B must be >= 0");
-  if (B == 0) return MLA_OK;
-  REQUIRE(q_cat && cache && block_table && seq_lens && o_lat && lse, "NULL tensor argument");
-  REQUIRE(max_pages > 0 && num_pages > 0, "max_pages and num_pages must be > 0");
-  REQUIRE(dims->d_c % 32 == 0 && dims->d_c <= 512, "d_c must be a multiple of 32, <= 512");
-  const int path = pick_path(dtype, dims);
-  const int workers = workers_for(path);
-  if (workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
-  const WorkspaceLayout L = workspace_layout(B, workers, dims->n_h, dims->d_c);
-  if (!workspace || ws_bytes < L.total)
-    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L.total);
-  (void)seq_lens;  // the plan in the workspace carries the validated lengths
-  if (path == 1)
-    return cuda_status(tc_pair_launch(q_cat, cache, block_table, max_pages, num_pages, B,
-                                      workers, softmax_scale, workspace, L, o_lat, lse,
-                                      dev_status, S(stream)),
-                       "decode_attn (tcgen05 pair)");
-  return cuda_status(launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, B,
-                                        workers, softmax_scale, workspace, L, o_lat, lse,
-                                        dims->n_h, dims->d_c, dims->d_r, dims->page_size,
-                                        dtype == MLA_F32, dev_status, S(stream)),
-                     "decode_attn (simt)");
+  DecodeSetup ds;
+  mla_status st = decode_setup(q_cat, cache, block_table, max_pages, num_pages, seq_lens, B,
+                               o_lat, lse, dtype, dims, &ds);
+  if (st != MLA_OK || B == 0) return st;
+  if (!workspace || ws_bytes < ds.L.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, ds.L.total);
+  // the plan in the workspace carries the validated lengths
+  return cuda_status(launch_decode(ds, q_cat, cache, block_table, max_pages, num_pages, B,
+                                   softmax_scale, workspace, o_lat, lse, dtype, dims, dev_status,
+                                   S(stream)),
+                     ds.path == 1 ? "decode_attn (tcgen05 pair)" : "decode_attn (simt)");
 }
 
 mla_status mla_combine(const void* workspace, size_t ws_bytes, int B, float* o_lat, float* lse,

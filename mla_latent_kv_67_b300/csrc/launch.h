@@ -51,6 +51,28 @@ cudaError_t launch_combine(const void* ws, const WorkspaceLayout& L, int B, int 
 
 mla_status record_error(mla_status st, const char* msg);
 
+// Host-side checks and dispatch shared by the decode entry points (api.cu).
+mla_status check_dims(const mla_dims* d);
+mla_status check_dtype(int dt);
+int pick_path(mla_dtype dt, const mla_dims* d);  // 1 tcgen05, 0 SIMT
+int workers_for(int path);                       // workers the plan cuts the pages into
+struct DecodeSetup {
+  int path, workers;
+  WorkspaceLayout L;
+};
+// Validates the arguments of a decode call exactly as mla_decode_attn does
+// and picks its kernel, worker count and workspace layout. B == 0 is valid
+// (nothing to do; `out` then has workers == 0).
+mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* block_table,
+                        int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                        const float* o_lat, const float* lse, mla_dtype dtype,
+                        const mla_dims* dims, DecodeSetup* out);
+// The decode kernel `ds` selects, on workspace `ws` (planned by launch_plan).
+cudaError_t launch_decode(const DecodeSetup& ds, const void* q_cat, const void* cache,
+                          const int32_t* block_table, int max_pages, int num_pages, int B,
+                          float softmax_scale, void* ws, float* o_lat, float* lse, mla_dtype dtype,
+                          const mla_dims* d, int32_t* dev_status, cudaStream_t s);
+
 // Raises a kernel's dynamic shared-memory limit once per device, so later
 // launches (including ones recorded into a CUDA graph) make no further host
 // API call for it. `done` is the caller's per-kernel bit mask of devices.

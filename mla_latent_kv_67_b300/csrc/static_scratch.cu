@@ -1,11 +1,10 @@
 // Allocation-free decode: mla_decode_attn_static.
 //
 // Some callers cannot allocate device memory at the point where they decode:
-// code running under a CUDA stream capture in global mode (cudaMalloc is not
-// permitted there), plugin hosts and embedded runtimes that hand a plugin a
-// stream but no allocator, and serving loops that forbid driver allocations
-// after start-up so that no step ever blocks on the allocator. Such a caller
-// has no way to provide the decode workspace. This entry point instead keeps
+// plugin hosts and embedded runtimes that hand a plugin a stream but no
+// allocator, and serving loops that forbid device allocations after
+// start-up so that no step ever blocks on the allocator. Such a caller has
+// no way to provide the decode workspace. This entry point instead keeps
 // that workspace (split plan plus split-KV partial results) in one
 // file-scope device array of fixed size, so the call itself allocates
 // nothing; the caller still provides every input and output tensor.
@@ -65,31 +64,16 @@ extern "C" mla_status mla_decode_attn_static(const void* q_cat, const void* cach
                                              mla_dtype dtype, const mla_dims* d,
                                              int32_t* dev_status, void* stream) {
   using namespace mla;
-  if (!d) return err(MLA_ERR_INVALID_ARG, "dims is NULL");
-  if (dtype != MLA_F32 && dtype != MLA_BF16) return err(MLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
-  if (d->n_h <= 0 || d->d_c <= 0 || d->d_h <= 0 || d->d_v <= 0 || d->page_size <= 0 ||
-      d->d_r < 0 || d->d_r % 2)
-    return err(MLA_ERR_INVALID_ARG, "bad dims");
-  if (B < 0) return err(MLA_ERR_INVALID_ARG, "B must be >= 0");
-  if (B == 0) return MLA_OK;
-  if (!q_cat || !cache || !block_table || !seq_lens || !o_lat || !lse)
-    return err(MLA_ERR_INVALID_ARG, "NULL tensor argument");
-  if (max_pages <= 0 || num_pages <= 0)
-    return err(MLA_ERR_INVALID_ARG, "max_pages and num_pages must be > 0");
-  if (d->d_c % 32 != 0 || d->d_c > 512)
-    return err(MLA_ERR_INVALID_ARG, "d_c must be a multiple of 32, <= 512");
-  const int path = mla_decode_path(dtype, d);
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-    return err(MLA_ERR_CUDA, "cannot query the device's SM count");
-  const int workers = path == 1 ? tc_pair_workers(sms) : sms;
-  const WorkspaceLayout L = workspace_layout(B, workers, d->n_h, d->d_c);
-  if (L.total > (size_t)MLA_STATIC_SCRATCH_BYTES)
+  // the same checks, kernel choice and plan layout as mla_decode_attn
+  DecodeSetup ds;
+  mla_status st = decode_setup(q_cat, cache, block_table, max_pages, num_pages, seq_lens, B,
+                               o_lat, lse, dtype, d, &ds);
+  if (st != MLA_OK || B == 0) return st;
+  if (ds.L.total > (size_t)MLA_STATIC_SCRATCH_BYTES)
     return err(MLA_ERR_WORKSPACE,
                "this batch needs %zu bytes of decode scratch (B=%d, %d workers, n_h=%d, d_c=%d) "
                "but the static scratch holds %zu; use mla_decode_attn with a caller workspace",
-               L.total, B, workers, d->n_h, d->d_c, (size_t)MLA_STATIC_SCRATCH_BYTES);
+               ds.L.total, B, ds.workers, d->n_h, d->d_c, (size_t)MLA_STATIC_SCRATCH_BYTES);
   void* ws = nullptr;
   cudaError_t e = scratch_address(&ws);
   if (e != cudaSuccess)
@@ -98,17 +82,12 @@ extern "C" mla_status mla_decode_attn_static(const void* q_cat, const void* cach
   // Nothing in the scratch needs to start at zero: the plan kernel rewrites
   // every plan entry it reads back, and each partial slot is written by the
   // decode kernel before the combine kernel reads it.
-  e = launch_plan(seq_lens, B, max_pages, d->page_size, workers, path, ws, L, dev_status, s);
-  if (e == cudaSuccess) {
-    if (path == 1)
-      e = tc_pair_launch(q_cat, cache, block_table, max_pages, num_pages, B, workers,
-                         softmax_scale, ws, L, o_lat, lse, dev_status, s);
-    else
-      e = launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, B, workers,
-                             softmax_scale, ws, L, o_lat, lse, d->n_h, d->d_c, d->d_r,
-                             d->page_size, dtype == MLA_F32, dev_status, s);
-  }
-  if (e == cudaSuccess) e = launch_combine(ws, L, B, d->n_h, d->d_c, o_lat, lse, s);
+  e = launch_plan(seq_lens, B, max_pages, d->page_size, ds.workers, ds.path, ws, ds.L, dev_status,
+                  s);
+  if (e == cudaSuccess)
+    e = launch_decode(ds, q_cat, cache, block_table, max_pages, num_pages, B, softmax_scale, ws,
+                      o_lat, lse, dtype, d, dev_status, s);
+  if (e == cudaSuccess) e = launch_combine(ws, ds.L, B, d->n_h, d->d_c, o_lat, lse, s);
   if (e != cudaSuccess) return err(MLA_ERR_CUDA, "decode_attn_static: %s", cudaGetErrorString(e));
   return MLA_OK;
 }

@@ -1,6 +1,6 @@
 """Expected values for a workload's sequences, computed by the fp64 oracle
-from the seeded inputs. Imports only ``oracle`` and ``synth`` (never the CUDA
-path)."""
+from the seeded inputs, and the parity gate that compares the GPU's outputs
+with them. Imports only ``oracle`` and ``synth`` (never the CUDA path)."""
 from __future__ import annotations
 
 import numpy as np
@@ -8,10 +8,59 @@ import numpy as np
 from oracle import mla_oracle as O
 from mla_latent_kv_67_b300 import synth
 
+# Tolerances of the parity gate.
+#  * Tensors (o_lat, o, u): max |gpu - ref| / max |ref| -- 1e-5 on the fp32
+#    path, 2e-2 on the bf16 path (bf16 cache and weights, bf16 q_cat and
+#    probabilities, fp32 accumulation).
+#  * lse (natural log of the softmax normaliser) is gated on its ABSOLUTE
+#    error, since an error in it is an error of the normaliser itself. A
+#    simulation of the bf16 roundings in fp64 (q_abs rounded to bf16 for the
+#    attention-only workloads; c_Q, q, q_cat and the appended row rounded as
+#    well on the full-layer workload) gives |d lse| of 2.7e-4 and 1.2e-3; the
+#    gates sit well above those and well below the 1e-2 that one dropped
+#    64-token page of a 4096-token context moves lse by.
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+LSE_ABS = {"f32": 1e-5, "bf16": 2e-3, "bf16_layer": 5e-3}
+
 
 def rel_to_max(got, ref) -> float:
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     return float(np.max(np.abs(got - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def lse_tol(wl: synth.Workload) -> float:
+    if wl.dtype == "f32":
+        return LSE_ABS["f32"]
+    return LSE_ABS["bf16_layer"] if wl.mode == "layer" else LSE_ABS["bf16"]
+
+
+def gate_errors(got: dict, ref: dict, explicit_heads=None) -> dict:
+    """Errors of one sequence's GPU outputs ``got`` (host arrays: any of
+    o_lat [n_h, d_c], o [n_h, d_v], lse [n_h], u [d_model]) against the
+    oracle's ``ref`` (from :meth:`Expected.seq`)."""
+    errs = {}
+    for k in ("o_lat", "o", "u"):
+        if k in got:
+            errs[k] = rel_to_max(got[k], ref[k])
+    if "o" in got and explicit_heads is not None and "o_explicit" in ref:
+        errs["o_explicit"] = rel_to_max(np.asarray(got["o"])[list(explicit_heads)],
+                                        ref["o_explicit"])
+    if "lse" in got:
+        errs["lse_abs"] = float(np.max(np.abs(np.asarray(got["lse"], np.float64) - ref["lse"])))
+        if explicit_heads is not None and "lse_explicit" in ref:
+            errs["lse_explicit_abs"] = float(np.max(np.abs(
+                np.asarray(got["lse"], np.float64)[list(explicit_heads)] - ref["lse_explicit"])))
+    return errs
+
+
+def gate_failures(errs: dict, tol: float, lse_abs: float) -> list[str]:
+    """The gate's verdict: the names of the errors above their bound."""
+    bad = []
+    for k, v in errs.items():
+        bound = lse_abs if k.startswith("lse") else tol
+        if not v <= bound:
+            bad.append(f"{k}={v:.3g}>{bound:g}")
+    return bad
 
 
 class Expected:
@@ -66,12 +115,19 @@ class Expected:
             c, k = np.concatenate([c, c2]), np.concatenate([k, k2])
         return c, k
 
-    def seq(self, b: int, explicit_heads=None):
+    def seq(self, b: int, explicit_heads=None, drop_rows=None):
         """Oracle outputs of sequence b: absorbed (all heads) and, for
-        ``explicit_heads``, the explicit non-absorbed definition."""
+        ``explicit_heads``, the explicit non-absorbed definition.
+        ``drop_rows`` (a slice of token indices) removes those cached tokens
+        from the oracle's input: a planted mistake for checking that the
+        parity gate rejects a wrong answer."""
         wl = self.wl
         q_c, q_r = self.query(b)
         c, k = self.cache_rows(b)
+        if drop_rows is not None:
+            keep = np.ones(len(c), bool)
+            keep[drop_rows] = False
+            c, k = c[keep], k[keep]
         o, o_lat, lse = O.attention_absorbed(q_c, q_r, c, k, self.w["w_uk"], self.w["w_uv"], wl.scale)
         out = dict(o=o, o_lat=o_lat, lse=lse, q_c=q_c, q_r=q_r)
         if explicit_heads is not None:

@@ -1,10 +1,12 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
 the same seeded inputs.
 
-Tolerances (from the stated precision of each path):
+Tolerances (``tests/reference.py`` states them and their derivation):
   * fp32 path: max |gpu - ref| / max |ref| <= 1e-5;
   * bf16 path (bf16 cache and weights, bf16 q_cat and probabilities, fp32
-    accumulation): max |gpu - ref| / max |ref| <= 2e-2.
+    accumulation): max |gpu - ref| / max |ref| <= 2e-2;
+  * lse: an absolute bound (1e-5 fp32; 2e-3 bf16; 5e-3 on the full-layer
+    workload, whose query passes through three more bf16 roundings).
 """
 import numpy as np
 import pytest
@@ -13,11 +15,11 @@ import torch
 from mla_latent_kv_67_b300 import binding as M
 from mla_latent_kv_67_b300 import synth
 from mla_latent_kv_67_b300.step import DecodeStep
-from reference import Expected, rel_to_max
+from reference import (Expected, TOL, gate_errors, gate_failures, lse_tol, rel_to_max)
 
 pytestmark = pytest.mark.gpu
 
-TOL_F32, TOL_BF16 = 1e-5, 2e-2
+TOL_F32, TOL_BF16 = TOL["f32"], TOL["bf16"]
 
 
 def run(wl, **kw):
@@ -28,23 +30,26 @@ def run(wl, **kw):
     return st
 
 
+def host_outputs(st, b, what=("o_lat", "o", "lse")):
+    """Sequence b's GPU outputs as host float64 arrays."""
+    wl = st.wl
+    got = {}
+    if "o_lat" in what:
+        got["o_lat"] = st.o_lat[b].double().cpu().numpy()
+    if "o" in what:
+        got["o"] = st.o[b].double().cpu().numpy().reshape(wl.n_h, wl.d_v)
+    if "lse" in what:
+        got["lse"] = st.lse[b].double().cpu().numpy()
+    if "u" in what:
+        got["u"] = st.u[b].double().cpu().numpy()
+    return got
+
+
 def check_seq(st, ex, b, tol, explicit_heads=None, what=("o_lat", "o", "lse")):
     e = ex.seq(b, explicit_heads=explicit_heads)
-    errs = {}
-    if "o_lat" in what:
-        errs["o_lat"] = rel_to_max(st.o_lat[b].cpu().numpy(), e["o_lat"])
-    if "o" in what:
-        o = st.o[b].float().cpu().numpy().reshape(st.wl.n_h, st.wl.d_v)
-        errs["o"] = rel_to_max(o, e["o"])
-        if explicit_heads is not None:
-            errs["o_explicit"] = rel_to_max(o[list(explicit_heads)], e["o_explicit"])
-    if "lse" in what:
-        errs["lse"] = float(np.max(np.abs(st.lse[b].cpu().numpy() - e["lse"]))
-                            / max(1.0, np.max(np.abs(e["lse"]))))
-    if "u" in what:
-        errs["u"] = rel_to_max(st.u[b].cpu().numpy(), e["u"])
-    for k, v in errs.items():
-        assert v <= tol, f"seq {b}: {k} error {v:.3g} > {tol:g} ({errs})"
+    errs = gate_errors(host_outputs(st, b, what), e, explicit_heads)
+    bad = gate_failures(errs, tol, lse_tol(st.wl))
+    assert not bad, f"seq {b}: {bad} ({errs})"
     return errs
 
 
@@ -169,36 +174,56 @@ def test_bf16_sequence_split_over_32_ways():
 
 
 # ---------------------------------------------------- full-size workloads
-def _sampled(name, seqs, explicit_heads, what=("o_lat", "o", "lse")):
+def _full(name, explicit_seqs, explicit_heads, what=("o_lat", "o", "lse")):
+    """Every sequence and every head of a full-size workload against the
+    absorbed fp64 oracle; the explicit (non-absorbed) oracle on the sampled
+    sequences and heads. Returns the run, the oracle and the worst errors."""
     wl = synth.WORKLOADS[name]
     st = run(wl)
     ex = Expected(wl)
     worst = {}
-    for b in seqs:
-        errs = check_seq(st, ex, b, TOL_BF16, explicit_heads=explicit_heads, what=what)
+    for b in range(wl.batch):
+        eh = explicit_heads if b in explicit_seqs else None
+        errs = check_seq(st, ex, b, TOL_BF16, explicit_heads=eh, what=what)
         for k, v in errs.items():
             worst[k] = max(worst.get(k, 0.0), v)
-    o = st.result()
-    assert torch.isfinite(o).all()
-    return worst
+    print(name, {k: f"{v:.3g}" for k, v in worst.items()})
+    return st, ex, worst
 
 
 @pytest.mark.slow
 def test_full_dsv2_b32_ctx4k():
-    print(_sampled("dsv2_b32_ctx4k", range(0, 32, 3), explicit_heads=[0, 101]))
+    """All 32 sequences; and the gate itself must reject two planted wrong
+    answers on the same GPU output: the oracle with one 64-token page of one
+    sequence left out, and the oracle with two heads swapped."""
+    st, ex, _ = _full("dsv2_b32_ctx4k", (0, 13, 31), [0, 101])
+    tol_l = lse_tol(st.wl)
+    for b, page in ((3, 10), (17, 63)):
+        got = host_outputs(st, b)
+        wrong = ex.seq(b, drop_rows=slice(64 * page, 64 * page + 64))
+        errs = gate_errors(got, wrong)
+        assert gate_failures(errs, TOL_BF16, tol_l), f"a dropped page passed the gate: {errs}"
+        assert errs["lse_abs"] > tol_l and errs["o_lat"] > TOL_BF16, errs
+        right = ex.seq(b)
+        swapped = dict(right)
+        for k in ("o", "o_lat", "lse"):
+            v = right[k].copy()
+            v[[5, 90]] = v[[90, 5]]
+            swapped[k] = v
+        errs = gate_errors(got, swapped)
+        assert errs["o"] > TOL_BF16 and errs["o_lat"] > TOL_BF16 and errs["lse_abs"] > tol_l, errs
 
 
 @pytest.mark.slow
 def test_full_dsv2_b4_ctx128k():
-    print(_sampled("dsv2_b4_ctx128k", range(4), explicit_heads=[64]))
+    _full("dsv2_b4_ctx128k", range(4), [64])
 
 
 @pytest.mark.slow
 def test_full_dsv2_b128_ragged():
-    print(_sampled("dsv2_b128_ragged", [0, 1, 63, 127], explicit_heads=[3]))
+    _full("dsv2_b128_ragged", (0, 1, 63, 127), [3])
 
 
 @pytest.mark.slow
 def test_full_dsv2_layer_b64_ctx32k():
-    print(_sampled("dsv2_layer_b64_ctx32k", [0, 63], explicit_heads=[9],
-                   what=("o_lat", "o", "lse", "u")))
+    _full("dsv2_layer_b64_ctx32k", (0, 63), [9], what=("o_lat", "o", "lse", "u"))

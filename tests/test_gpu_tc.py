@@ -7,7 +7,7 @@ import torch
 from mla_latent_kv_67_b300 import binding as M
 from mla_latent_kv_67_b300 import synth
 from mla_latent_kv_67_b300.step import DecodeStep
-from reference import Expected, rel_to_max
+from reference import LSE_ABS, Expected, rel_to_max
 
 pytestmark = pytest.mark.gpu
 
@@ -70,7 +70,7 @@ def test_tc_matches_simt_and_oracle():
         e = ex.seq(i)
         err = rel_to_max(a.o_lat[i].cpu().numpy(), e["o_lat"])
         lerr = np.max(np.abs(a.lse[i].cpu().numpy() - e["lse"]))
-        assert err < 2e-2 and lerr < 2e-2, (i, err, lerr)
+        assert err < 2e-2 and lerr < LSE_ABS["bf16"], (i, err, lerr)
 
 
 def test_tc_timeout_free_on_idle_workers():

@@ -32,7 +32,7 @@ def _rank(rank, world, port, out):
     buf = io.StringIO()
     args = bench.argparse.Namespace(impl="reference", gpus=world, steps=1, warmup=0,
                                     workload="tiny_f32_ctx256", no_cpu_baseline=True,
-                                    cpu_seconds=1.0)
+                                    no_other=True)
     rc = None
     if rank != 0:
         with contextlib.redirect_stdout(buf):
@@ -64,3 +64,18 @@ def test_single_process_is_identity():
     import bench
     assert not dist.is_initialized()
     assert bench.max_over_ranks([3, 4.5], torch.device("cpu")) == [3.0, 4.5]
+
+
+def test_reference_arm_times_whole_oracle_steps(capsys):
+    """Rank 0 alone: each timed step is one whole oracle step, so the
+    reported time per step times the step count fits inside the run."""
+    import json
+    import bench
+    args = bench.argparse.Namespace(impl="reference", gpus=1, steps=3, warmup=1,
+                                    workload="tiny_f32_ctx256", no_cpu_baseline=True,
+                                    no_other=True)
+    assert bench.run_reference(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "us/step"
+    assert line["ms_per_step"] * line["steps"] / 1e3 <= line["wall_s"]
+    assert line["cpu_baseline"]["value"] == line["value"] == line["e2e"]["value"]

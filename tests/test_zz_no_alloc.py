@@ -1,10 +1,12 @@
 """The allocation-free decode entry point (mla_decode_attn_static).
 
-Callers that cannot allocate device memory while decoding (stream capture in
-global mode, plugin hosts without an allocator, serving loops that ban
-allocations after start-up) use this call instead of the workspace one. It
-must give the same results as mla_decode_attn + mla_combine with a caller
-workspace, call after call, and refuse a batch too large for its fixed
+Some callers cannot hand the library a workspace: a plugin host or embedded
+runtime that passes a stream but no allocator, or a serving loop that bans
+device allocations once it has started so that no step ever waits on the
+allocator. They call mla_decode_attn_static, which keeps the plan and the
+split partials in a fixed device array inside the library. It must give the
+same results as mla_decode_attn + mla_combine with a caller workspace, call
+after call, match the oracle, and refuse a batch too large for its fixed
 scratch with a clear error.
 
 This file is named so that pytest collects it after every other test.
@@ -17,7 +19,7 @@ import torch
 from mla_latent_kv_67_b300 import binding as M
 from mla_latent_kv_67_b300 import synth
 from mla_latent_kv_67_b300.step import DecodeStep
-from reference import rel_to_max
+from reference import Expected, gate_errors, gate_failures, lse_tol, rel_to_max
 
 pytestmark = pytest.mark.gpu
 
@@ -27,12 +29,19 @@ CASES = [
                    page_size=16, lens=(1, 33, 200, 517), dtype="f32", seed=901),
     synth.WORKLOADS["dsv2_b32_ctx4k"].replace(name="static_bf16", batch=5, n_h=16,
                                               lens=(1, 64, 300, 1500, 4096), seed=902),
+    # the DeepSeek-V2 shape: 128 heads, d_c 512, bf16 -> the tcgen05 pair
+    # kernel runs on the static scratch
+    synth.WORKLOADS["dsv2_b32_ctx4k"].replace(
+        name="static_dsv2_b32", lens=tuple([1, 64, 65, 4096] + [97 * i + 13 for i in range(1, 29)]),
+        seed=903),
 ]
 
 
 @pytest.mark.parametrize("wl", CASES, ids=lambda w: w.name)
 def test_static_scratch_matches_workspace_decode(wl):
     st = DecodeStep(wl)
+    if wl.n_h == 128 and wl.dtype == "bf16":
+        assert M.mla_decode_path(st.dtype, st.dims) == 1, "expected the tensor-core kernel"
     st.absorb_q()
     st.plan()
     st.attend()
@@ -50,6 +59,15 @@ def test_static_scratch_matches_workspace_decode(wl):
         err_o = rel_to_max(o.cpu().numpy(), ref_o.cpu().numpy())
         err_l = rel_to_max(l.cpu().numpy(), ref_l.cpu().numpy())
         assert err_o <= TOL[wl.dtype] and err_l <= TOL[wl.dtype], (call, err_o, err_l)
+        if wl.n_h == 128:
+            # same plan, same kernels: the same bits as the workspace path
+            assert torch.equal(o, ref_o) and torch.equal(l, ref_l), call
+    if wl.n_h == 128:
+        ex = Expected(wl)
+        for b in range(wl.batch):
+            got = {"o_lat": o[b].double().cpu().numpy(), "lse": l[b].double().cpu().numpy()}
+            errs = gate_errors(got, ex.seq(b))
+            assert not gate_failures(errs, TOL["bf16"], lse_tol(wl)), (b, errs)
 
 
 def test_static_scratch_refuses_a_plan_that_does_not_fit():
