@@ -38,6 +38,19 @@ mla_status cuda_status(cudaError_t e, const char* what) {
 
 cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// A projection: the tcgen05 weight-streaming GEMM for bf16 operands of a
+// shape it takes, the CUDA-core GEMM otherwise (fp32, odd K, or the SIMT
+// path forced for cross-checks).
+cudaError_t projection(const GemmArgs& g, cudaStream_t s) {
+  if (!g.a_f32 && !g.w_f32 && g.G == 1 && g.w_ks == 1 && g_forced_path != 0 &&
+      aligned16(g.a) && aligned16(g.w) && g.w_ns % 8 == 0 &&
+      tc_gemm_supported(g.M, g.N, g.K, g.a_ms))
+    return tc_gemm_launch(g, g.a_ms, s);
+  return launch_simt_gemm(g, s);
+}
+
 }  // namespace
 
 namespace mla {
@@ -182,7 +195,7 @@ mla_status mla_append_latent(const void* x, const void* w_dkv_kr, const int32_t*
   g.rope_period = g.N; g.pos = pos;
   g.seq_idx = seq_idx; g.block_table = block_table; g.B = B; g.max_pages = max_pages;
   g.num_pages = num_pages; g.page_size = dims->page_size; g.dev_status = dev_status;
-  return cuda_status(launch_simt_gemm(g, S(stream)), "append_latent");
+  return cuda_status(projection(g, S(stream)), "append_latent");
 }
 
 mla_status mla_project_q(const void* x, const void* w_dq, const void* w_uq_qr,
@@ -207,7 +220,7 @@ mla_status mla_project_q(const void* x, const void* w_dq, const void* w_uq_qr,
     g.w = w_dq; g.w_ns = dims->d_model; g.w_ks = 1; g.w_f32 = f32;
     g.G = 1; g.M = T; g.N = dims->d_cq; g.K = dims->d_model;
     g.epi = EPI_STORE; g.out = c_q; g.o_ms = dims->d_cq; g.o_f32 = f32;
-    if ((st = cuda_status(launch_simt_gemm(g, S(stream)), "project_q/W^DQ")) != MLA_OK) return st;
+    if ((st = cuda_status(projection(g, S(stream)), "project_q/W^DQ")) != MLA_OK) return st;
     src = c_q;
     K = dims->d_cq;
   }
@@ -219,7 +232,7 @@ mla_status mla_project_q(const void* x, const void* w_dq, const void* w_uq_qr,
   g.epi = EPI_ROPE; g.out = q; g.o_ms = g.N; g.o_f32 = f32;
   g.rope = rope; g.max_pos = max_pos; g.d_r = dims->d_r; g.rope_off = dims->d_h;
   g.rope_period = per_head; g.pos = pos; g.dev_status = dev_status;
-  return cuda_status(launch_simt_gemm(g, S(stream)), "project_q/W^UQ|W^QR");
+  return cuda_status(projection(g, S(stream)), "project_q/W^UQ|W^QR");
 }
 
 mla_status mla_absorb_q(const void* q, const void* w_uk, void* q_cat, int B, mla_dtype dtype,
@@ -375,7 +388,7 @@ mla_status mla_out_proj(const void* o, const void* w_o, float* u, int B, mla_dty
   g.w = w_o; g.w_ns = K; g.w_ks = 1; g.w_f32 = dtype == MLA_F32;
   g.G = 1; g.M = B; g.N = dims->d_model; g.K = K;
   g.epi = EPI_STORE; g.out = u; g.o_ms = dims->d_model; g.o_f32 = 1;
-  return cuda_status(launch_simt_gemm(g, S(stream)), "out_proj");
+  return cuda_status(projection(g, S(stream)), "out_proj");
 }
 
 }  // extern "C"

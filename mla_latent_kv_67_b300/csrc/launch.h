@@ -33,6 +33,11 @@ struct GemmArgs {
 };
 
 cudaError_t launch_simt_gemm(const GemmArgs& g, cudaStream_t s);
+// tcgen05 weight-streaming version of the same product for G == 1, bf16 A
+// and W, W K-major (w_ks == 1), K % 64 == 0 (tc_gemm.cu). `ldx` is A's row
+// stride in elements.
+bool tc_gemm_supported(int M, int N, int K, long long ldx);
+cudaError_t tc_gemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s);
 cudaError_t launch_copy_rope_part(const void* q, void* q_cat, int B, int n_h, int d_h, int d_r,
                                   int d_c, int f32, cudaStream_t s);
 cudaError_t launch_rope_table(float* cs, int max_pos, int d_r, double base, cudaStream_t s);

@@ -13,14 +13,18 @@ from mla_latent_kv_67_b300 import synth
 #    path, 2e-2 on the bf16 path (bf16 cache and weights, bf16 q_cat and
 #    probabilities, fp32 accumulation).
 #  * lse (natural log of the softmax normaliser) is gated on its ABSOLUTE
-#    error, since an error in it is an error of the normaliser itself. A
-#    simulation of the bf16 roundings in fp64 (q_abs rounded to bf16 for the
-#    attention-only workloads; c_Q, q, q_cat and the appended row rounded as
-#    well on the full-layer workload) gives |d lse| of 2.7e-4 and 1.2e-3; the
-#    gates sit well above those and well below the 1e-2 that one dropped
-#    64-token page of a 4096-token context moves lse by.
+#    error, since an error in it is an error of the normaliser itself. The
+#    bf16 rounding of q_abs moves every score s_j by scale * (dq . c_j); lse
+#    moves by the p-weighted mean of those shifts, which is largest when one
+#    token dominates (a one-token context: lse = s_0). A simulation of the
+#    bf16 roundings in fp64 gives a worst |d lse| of 4.9e-3 on attention-only
+#    workloads (q_abs rounded) and 9.0e-3 on the full layer (c_Q, q, q_cat
+#    and the appended row rounded as well), both at one-token contexts, and
+#    2.7e-4 / 1.2e-3 at 4096 tokens. The gates sit at twice the worst case;
+#    one dropped 64-token page of a 4096-token context moves lse by 0.023 to
+#    0.028 (max over heads), which the attention-only gate rejects.
 TOL = {"f32": 1e-5, "bf16": 2e-2}
-LSE_ABS = {"f32": 1e-5, "bf16": 2e-3, "bf16_layer": 5e-3}
+LSE_ABS = {"f32": 1e-5, "bf16": 1e-2, "bf16_layer": 2e-2}
 
 
 def rel_to_max(got, ref) -> float:
