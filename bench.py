@@ -52,7 +52,8 @@ DEFAULT_WORKLOAD = "dsv2_b32_ctx4k"
 # capture of that kernel on the workload. Valid only for the kernel source
 # the capture measured: drop the entry whenever the decode kernel changes,
 # until it is captured again.
-DECODE_TRAFFIC = {"dsv2_b32_ctx4k": 157_475_840 + 5_623_296}
+DECODE_TRAFFIC = {}
+DECODE_KERNELS = {0: "simt", 1: "tcgen05 latent-split pair", 2: "tcgen05 score/value pair"}
 
 
 def parse():
@@ -375,7 +376,7 @@ def measure_workload(wl, dev, K, W, flush, stream, hbm, tflops, barrier=None, sa
             "roofline_us": max(t_hbm, t_flop) * 1e6,
             "frac_of_roofline": max(t_hbm, t_flop) * 1e6 / kernel_us}
     return st, g, {"step_us": step_ms * 1e3, "stages_us": stages, "roofline": roof,
-                   "decode_kernel": "tcgen05" if path == 1 else "simt",
+                   "decode_kernel": DECODE_KERNELS.get(path, "simt"),
                    "step_roofline": step_roofline(wl, st.lens_np, hbm, tflops, step_ms * 1e3)}
 
 
@@ -502,7 +503,7 @@ def main():
     roof["frac_of_roofline"] = roof["roofline_us"] / (kernel_ms * 1e3)
     roof["peak_source"] = peak_kind
     roof["timing"] = "decode launch alone in its own CUDA graph, L2 flushed before each"
-    launches = sum({"absorb_q": 1 if res["decode_kernel"] == "tcgen05" else 2,
+    launches = sum({"absorb_q": 1 if res["decode_kernel"] != "simt" else 2,
                     "project": 2 if wl.d_cq else 1}.get(f.__name__, 1) for f in stages)
     line = {
         "metric": METRIC, "value": step_ms * 1e3, "unit": UNIT, "n_gpus": world, "steps": K,

@@ -240,13 +240,17 @@ mla_status mla_tc_selftest(const void* q_cat, const void* page, const void* pmat
                            float* o_out, int half, int32_t* dev_status, void* stream);
 
 /* Which decode kernel the given dtype/dims select on the current device:
- * 1 = tcgen05 tensor-core kernel, 0 = CUDA-core (SIMT) kernel. */
+ * 1 = tcgen05 tensor-core kernel (each SM of a pair owns half of d_c),
+ * 2 = the older tcgen05 score/value pair kernel (only when forced),
+ * 0 = CUDA-core (SIMT) kernel. */
 int mla_decode_path(mla_dtype dtype, const mla_dims* dims);
 
-/* Pin the decode kernel choice for this process: 0 = always the SIMT kernel,
- * 1 = the tcgen05 kernel wherever it supports the shape, -1 = automatic
- * (default). Plans, workspaces and decode calls must be made under the same
- * setting. Used to cross-check the two kernels against each other. */
+/* Pin the decode kernel choice for this process: 0 = always the SIMT kernel
+ * (and the CUDA-core GEMMs), 1 = the tcgen05 kernels wherever they support
+ * the shape, 2 = as 1 but the score/value pair decode kernel, -1 =
+ * automatic (default, same as 1). Plans, workspaces and decode calls must be
+ * made under the same setting. Used to cross-check the kernels against each
+ * other. */
 void mla_force_decode_path(int path);
 
 #ifdef __cplusplus

@@ -15,6 +15,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libmla_b300.so")
+# The same sources compiled with MLA_TEST_HOOKS: shortened device wait
+# limits and mla_test_withhold_pages (include/mla_b300_test.h), for the
+# tests that make a bounded wait run out. Never the shipped library.
+HOOK_LIB = os.path.join(LIBDIR, "libmla_b300_testhooks.so")
 OBJDIR = os.path.join(os.path.dirname(HERE), "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -32,18 +36,23 @@ def _newest_header() -> float:
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def build(ptxas_verbose: bool = False, force: bool = False, quiet: bool = True) -> str:
+def build(ptxas_verbose: bool = False, force: bool = False, quiet: bool = True,
+          hooks: bool = False) -> str:
+    lib = HOOK_LIB if hooks else LIB
+    objdir = os.path.join(OBJDIR, "hooks") if hooks else OBJDIR
     os.makedirs(LIBDIR, exist_ok=True)
-    os.makedirs(OBJDIR, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_t = _newest_header()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                     "--expt-relaxed-constexpr", "-I", os.path.dirname(HERE)]
     if ptxas_verbose:
         flags += ["-Xptxas", "-v"]
+    if hooks:
+        flags += ["-DMLA_TEST_HOOKS"]
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         if (not force and not ptxas_verbose and os.path.exists(obj)
                 and os.path.getmtime(obj) >= max(os.path.getmtime(src), hdr_t)):
             return obj, ""
@@ -59,16 +68,17 @@ def build(ptxas_verbose: bool = False, force: bool = False, quiet: bool = True) 
     if logs and (ptxas_verbose or not quiet):
         sys.stderr.write(logs)
     objs = [o for o, _ in results]
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + ".tmp"
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "shared",
                                                               "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(ptxas_verbose="--ptxas-v" in sys.argv, force="--force" in sys.argv, quiet=False))
+    print(build(ptxas_verbose="--ptxas-v" in sys.argv, force="--force" in sys.argv, quiet=False,
+                hooks="--hooks" in sys.argv))

@@ -83,13 +83,16 @@ int device_sms() {
 int pick_path(mla_dtype dt, const mla_dims* d) {
   if (g_forced_path == 0) return 0;
   const bool tc_ok = dt == MLA_BF16 && tc_decode_supported(d->n_h, d->d_c, d->d_r, d->page_size);
-  return tc_ok ? 1 : 0;
+  if (!tc_ok) return 0;
+  return g_forced_path == 2 ? 2 : 1;
 }
 
 int workers_for(int path) {
   const int sms = device_sms();
   if (sms <= 0) return 0;
-  return path == 1 ? tc_pair_workers(sms) : sms;
+  if (path == 1) return tc_split_workers(sms);
+  if (path == 2) return tc_pair_workers(sms);
+  return sms;
 }
 
 
@@ -98,6 +101,9 @@ cudaError_t launch_decode(const DecodeSetup& ds, const void* q_cat, const void* 
                           float softmax_scale, void* ws, float* o_lat, float* lse, mla_dtype dtype,
                           const mla_dims* d, int32_t* dev_status, cudaStream_t s) {
   if (ds.path == 1)
+    return tc_split_launch(q_cat, cache, block_table, max_pages, num_pages, B, ds.workers,
+                           softmax_scale, ws, ds.L, o_lat, lse, dev_status, s);
+  if (ds.path == 2)
     return tc_pair_launch(q_cat, cache, block_table, max_pages, num_pages, B, ds.workers,
                           softmax_scale, ws, ds.L, o_lat, lse, dev_status, s);
   return launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, B, ds.workers,
@@ -145,7 +151,7 @@ const char* mla_last_error(void) { return g_last_error.c_str(); }
 int mla_abi_version(void) { return MLA_ABI_VERSION; }
 
 void mla_force_decode_path(int path) {
-  g_forced_path = (path == 0 || path == 1) ? path : -1;
+  g_forced_path = (path == 0 || path == 1 || path == 2) ? path : -1;
 }
 
 int mla_decode_path(mla_dtype dtype, const mla_dims* dims) {
@@ -303,7 +309,7 @@ mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* 
   return cuda_status(launch_decode(ds, q_cat, cache, block_table, max_pages, num_pages, B,
                                    softmax_scale, workspace, o_lat, lse, dtype, dims, dev_status,
                                    S(stream)),
-                     ds.path == 1 ? "decode_attn (tcgen05 pair)" : "decode_attn (simt)");
+                     ds.path == 0 ? "decode_attn (simt)" : "decode_attn (tcgen05)");
 }
 
 mla_status mla_combine(const void* workspace, size_t ws_bytes, int B, float* o_lat, float* lse,

@@ -265,7 +265,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int max_pages, int page_
                         cudaStream_t s) {
   // the tcgen05 kernel's per-sequence cost (Q fetch, O write-out) is worth
   // about four pages; the SIMT kernel's is small next to its page cost
-  const int c_seg = path == 1 ? 4 : 0;
+  const int c_seg = path >= 1 ? 4 : 0;
   plan_kernel<<<1, 1024, 0, s>>>(seq_lens, B, max_pages, page_size, workers, path, c_seg, (char*)ws,
                                  L, dev_status);
   return cudaGetLastError();

@@ -11,7 +11,13 @@ namespace mla {
 // Shapes the tensor-core kernel is built for (DeepSeek-V2 MLA: 128 heads,
 // 512-wide latent, 64-wide RoPE key, 64-token pages).
 bool tc_decode_supported(int n_h, int d_c, int d_r, int page_size);
-// The CTA-pair kernel (score CTA + value CTA per worker).
+// The latent-split pair kernel (each CTA of a cluster owns half of d_c).
+int tc_split_workers(int sms);
+cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t* block_table,
+                            int max_pages, int num_pages, int B, int workers, float scale,
+                            const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
+                            int32_t* dev_status, cudaStream_t s);
+// The score/value pair kernel (score CTA + value CTA per worker).
 int tc_pair_workers(int sms);
 cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* block_table,
                            int max_pages, int num_pages, int B, int workers, float scale,

@@ -79,14 +79,14 @@ RAGGED = synth.WORKLOADS["dsv2_b32_ctx4k"].replace(
     name="ragged_small", batch=6, lens=(1, 17, 64, 65, 64 * 5 + 17, 1000), seed=11)
 
 
-@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("path", [0, 1, 2])
 def test_bf16_ragged_small(path):
     """Several pages and ragged tails (1, 17, 64, 65, 337, 1000 tokens):
     every head against the absorbed oracle, three heads against the explicit
     definition."""
     M.mla_force_decode_path(path)
     try:
-        if path == 1 and M.mla_decode_path(M.MLA_BF16, M.Dims.of(RAGGED)) != 1:
+        if path >= 1 and M.mla_decode_path(M.MLA_BF16, M.Dims.of(RAGGED)) != path:
             pytest.skip("tensor-core decode kernel not available")
         st = run(RAGGED)
         ex = Expected(RAGGED)

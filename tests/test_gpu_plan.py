@@ -71,11 +71,11 @@ def check(lens, max_pages):
                 owner[(s, p)] = g
         assert len(got) == n, f"worker {g}: n_pages {n} != {len(got)}"
         order += got
-        c = C_SEG_TC if path == 1 else 0
+        c = C_SEG_TC if path >= 1 else 0
         costs.append(len(got) + c * segs)
     want = [(s, p) for s in range(B) for p in range(pages[s])]
     assert order == want, "pages not covered exactly once, in order"
-    c = C_SEG_TC if path == 1 else 0
+    c = C_SEG_TC if path >= 1 else 0
     assert max(costs) <= per + c, f"worker cost {max(costs)} > per {per} + {c}"
     # per-sequence split records and partial slots
     slot = 0
