@@ -156,7 +156,13 @@ __global__ void __launch_bounds__(THREADS)
 
   // ---------------------------------------------------------- epilogue
   // 1. every CTA's partial accumulator is complete and its ring is idle
-  const bool mma_ok = __all_sync(0xffffffffu, mbar_wait_bounded(done, 0, abort_flag, a.dev_status, WAIT_NS) && !*abort_flag);
+  // one lane per warp polls, sleeping between polls, so the waiting warps
+  // take no issue slots from the producer and the MMA issuer
+  bool waited = true;
+  if (lane == 0) waited = mbar_wait_sleepy(done, 0, abort_flag, a.dev_status, WAIT_NS, 64);
+  waited = __shfl_sync(0xffffffffu, waited, 0);
+  if (waited) mbar_try_wait(done, 0);  // each lane acquires the completed phase
+  const bool mma_ok = __all_sync(0xffffffffu, waited && !*abort_flag);
   tc_fence_after();
   const int R = TILE_N / cs;  // output features each CTA of the cluster owns
   float* red = reinterpret_cast<float*>(smem);  // [cs][mt][R], reuses the ring

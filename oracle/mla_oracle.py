@@ -17,6 +17,8 @@ It states what the decode path computes in the plainest form, in float64:
 * attention in the **absorbed** form (query folded through W^UK, softmax over
   the latent rows, latent output mapped back through W^UV), used as a cheap
   cross-check that covers every head of the large workloads;
+* decode of several new tokens at once (each sees the cache up to its own
+  position);
 * the log-sum-exp merge of attention over disjoint token subsets;
 * the output projection W^O;
 * the cache-size closed forms the pages print.
@@ -218,6 +220,36 @@ def attention_absorbed(q_c, q_r, c, k_r, w_uk, w_uv, scale: float):
     q_abs = absorb_query(q_c, w_uk)
     o_lat, lse = attention_latent(q_abs, q_r, c, k_r, scale)
     return absorb_output(o_lat, w_uv), o_lat, lse
+
+
+# ------------------------------------------------- multi-token decode
+def multi_token_lengths(n_cached: int, n_new: int) -> np.ndarray:
+    """Cached rows each of ``n_new`` new tokens attends over when they are
+    decoded together (multi-token prediction / speculative drafts, [MLA-V2]
+    4.3 and 6): the new tokens hold the last ``n_new`` of ``n_cached`` cache
+    positions, and token t sees every position up to and including its own,
+    ``n_cached - n_new + t + 1`` rows."""
+    assert 1 <= n_new <= n_cached
+    return n_cached - n_new + 1 + np.arange(n_new)
+
+
+def attention_multi_token(q_c, q_r, c, k_r, w_uk, w_uv, scale: float, form: str = "explicit"):
+    """Decode attention of ``T`` new tokens at once: token t attends over the
+    first :func:`multi_token_lengths` ``(N, T)[t]`` cached rows, the explicit
+    (or absorbed) single-token attention on that prefix.
+
+    ``q_c [T, n_h, d_h]``, ``q_r [T, n_h, d_R]``, ``c [N, d_c]``,
+    ``k_r [N, d_R]``. Returns ``o [T, n_h, d_v]`` and ``lse [T, n_h]``."""
+    T = len(q_c)
+    outs, lses = [], []
+    for t, n in enumerate(multi_token_lengths(len(c), T)):
+        if form == "explicit":
+            o, lse = attention_explicit(q_c[t], q_r[t], c[:n], k_r[:n], w_uk, w_uv, scale)
+        else:
+            o, _, lse = attention_absorbed(q_c[t], q_r[t], c[:n], k_r[:n], w_uk, w_uv, scale)
+        outs.append(o)
+        lses.append(lse)
+    return np.stack(outs), np.stack(lses)
 
 
 # ----------------------------------------------------- split-KV merge

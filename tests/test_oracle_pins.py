@@ -223,6 +223,78 @@ def check_mha_reduction_sdpa(attn=O.attention_explicit):
     return rel(o, ref.numpy()[:, 0, :])
 
 
+def check_multi_token_sdpa(attn=O.attention_multi_token, lengths=O.multi_token_lengths):
+    """MHA special case of decoding T new tokens together: the T queries sit
+    at the last T cache positions, so torch's fp64 scaled_dot_product_attention
+    with a boolean mask that lets query t see keys 0 .. N - T + t (a library
+    routine with the causal mask aligned to the end) must agree."""
+    n_h, d_h, d_r, N, T = 3, 4, 2, 23, 4
+    d_c = n_h * d_h
+    g = np.random.default_rng(17)
+    c, k_r = g.standard_normal((N, d_c)), g.standard_normal((N, d_r))
+    q_c, q_r = g.standard_normal((T, n_h, d_h)), g.standard_normal((T, n_h, d_r))
+    w_uk, w_uv = np.zeros((n_h * d_h, d_c)), np.zeros((n_h * d_h, d_c))
+    for h in range(n_h):
+        for i in range(d_h):
+            w_uk[h * d_h + i, h * d_h + (i + 1) % d_h] = 1.0
+            w_uv[h * d_h + i, h * d_h + (i + 2) % d_h] = 1.0
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    o, lse = attn(q_c, q_r, c, k_r, w_uk, w_uv, scale)
+    K = np.stack([np.concatenate([c @ w_uk[h * d_h:(h + 1) * d_h].T, k_r], axis=1)
+                  for h in range(n_h)])                               # [n_h, N, d_h + d_r]
+    V = np.stack([c @ w_uv[h * d_h:(h + 1) * d_h].T for h in range(n_h)])
+    Q = np.concatenate([q_c, q_r], axis=2).transpose(1, 0, 2)        # [n_h, T, d_h + d_r]
+    mask = np.arange(N)[None, :] <= (N - T + np.arange(T))[:, None]   # [T, N]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(Q), torch.from_numpy(K), torch.from_numpy(V),
+        attn_mask=torch.from_numpy(mask), scale=scale).numpy()        # [n_h, T, d_v]
+    err = rel(o, ref.transpose(1, 0, 2))
+    # lse: log sum_j exp(s_j) over the same visible keys
+    s = np.einsum("htd,hnd->htn", Q, K) * scale
+    s = np.where(mask[None], s, -np.inf)
+    ref_lse = np.log(np.exp(s - s.max(-1, keepdims=True)).sum(-1)) + s.max(-1)
+    return max(err, float(np.max(np.abs(lse - ref_lse.T))))
+
+
+def test_multi_token_decode_matches_masked_sdpa():
+    assert check_multi_token_sdpa() < 1e-12
+    assert list(O.multi_token_lengths(10, 3)) == [8, 9, 10]
+    assert list(O.multi_token_lengths(1, 1)) == [1]
+
+
+def test_multi_token_planted_mistakes_are_caught():
+    def top_left(n, t):  # token t sees rows 0..t (a mask aligned to the start)
+        return 1 + np.arange(t)
+
+    def without_own(n, t):  # token t does not see its own row
+        return n - t + np.arange(t)
+
+    for bad in (top_left, without_own):
+        def attn(q_c, q_r, c, k_r, w_uk, w_uv, scale, bad=bad):
+            outs, lses = [], []
+            for t, n in enumerate(bad(len(c), len(q_c))):
+                o, lse = O.attention_explicit(q_c[t], q_r[t], c[:n], k_r[:n], w_uk, w_uv, scale)
+                outs.append(o)
+                lses.append(lse)
+            return np.stack(outs), np.stack(lses)
+        assert check_multi_token_sdpa(attn) > 1e-3
+
+
+def test_multi_token_one_token_and_forms_agree():
+    case = tiny_case(n_h=2, N=9, seed=3)
+    o1, l1 = O.attention_explicit(**case)
+    om, lm = O.attention_multi_token(case["q_c"][None], case["q_r"][None], case["c"], case["k_r"],
+                                     case["w_uk"], case["w_uv"], case["scale"])
+    assert np.array_equal(om[0], o1) and np.array_equal(lm[0], l1)
+    g = np.random.default_rng(4)
+    q_c, q_r = g.standard_normal((3, 2, 3)), g.standard_normal((3, 2, 2))
+    oe, le = O.attention_multi_token(q_c, q_r, case["c"], case["k_r"], case["w_uk"], case["w_uv"],
+                                     case["scale"])
+    oa, la = O.attention_multi_token(q_c, q_r, case["c"], case["k_r"], case["w_uk"], case["w_uv"],
+                                     case["scale"], form="absorbed")
+    assert rel(oe, oa) < 1e-10 and np.max(np.abs(le - la)) < 1e-10
+
+
 def test_attention_brute_force():
     assert check_brute_force() < 1e-12
 
