@@ -80,14 +80,18 @@ def peaks():
 def algorithmic(wl, lens):
     """Algorithmic bytes and FLOPs of one decode_attn launch: each cached row
     (c_kv | k_R) read once, q_cat read once, o_lat written once; FLOPs of the
-    two contractions (scores over d_c + d_r, latent output over d_c)."""
+    two contractions (scores over d_c + d_r, latent output over d_c). With
+    q_len new tokens per sequence the rows are still read once, and new
+    token t of a sequence of length L attends over L - q_len + 1 + t rows."""
     esz = 2 if wl.dtype == "bf16" else 4
+    lens = np.asarray(lens, np.int64)
     tokens = int(np.sum(lens))
-    B = len(lens)
+    R = len(lens) * wl.q_len
+    seen = int(np.sum(lens)) * wl.q_len - len(lens) * (wl.q_len * (wl.q_len - 1) // 2)
     cache = tokens * (wl.d_c + wl.d_r) * esz
-    q = B * wl.n_h * (wl.d_c + wl.d_r) * esz
-    o = B * wl.n_h * wl.d_c * 4
-    flops = tokens * (2 * wl.n_h * (wl.d_c + wl.d_r) + 2 * wl.n_h * wl.d_c)
+    q = R * wl.n_h * (wl.d_c + wl.d_r) * esz
+    o = R * wl.n_h * wl.d_c * 4
+    flops = seen * (2 * wl.n_h * (wl.d_c + wl.d_r) + 2 * wl.n_h * wl.d_c)
     return cache + q + o, flops
 
 
@@ -281,6 +285,12 @@ def run_reference(args):
 def weight_bytes(wl):
     """Bytes of the weights one step of the workload reads (bf16 or fp32)."""
     esz = 2 if wl.dtype == "bf16" else 4
+    if wl.fused:
+        k = wl.d_cq or wl.d_model
+        n = (wl.d_c + wl.d_r) * wl.d_model + wl.d_cq * wl.d_model   # W^DKV | W^KR, W^DQ
+        n += wl.n_h * (wl.d_c + wl.d_r) * k                         # W^UK^T W^UQ | W^QR
+        n += wl.d_model * wl.n_h * wl.d_c                           # W^O W^UV
+        return n * esz, n
     n = wl.n_h * wl.d_h * wl.d_c + wl.n_h * wl.d_v * wl.d_c     # W^UK, W^UV
     if wl.mode == "layer":
         k = wl.d_cq or wl.d_model
@@ -504,7 +514,8 @@ def main():
     roof["peak_source"] = peak_kind
     roof["timing"] = "decode launch alone in its own CUDA graph, L2 flushed before each"
     launches = sum({"absorb_q": 1 if res["decode_kernel"] != "simt" else 2,
-                    "project": 2 if wl.d_cq else 1}.get(f.__name__, 1) for f in stages)
+                    "project": 2 if wl.d_cq else 1, "project_absorbed": 2 if wl.d_cq else 1,
+                    "out_absorbed": 2}.get(f.__name__, 1) for f in stages)
     line = {
         "metric": METRIC, "value": step_ms * 1e3, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False,
@@ -533,12 +544,13 @@ def main():
         for name in OTHER_WORKLOADS:
             if name == wl.name:
                 continue
-            ow = synth.WORKLOADS[name]
+            ow = synth.WORKLOADS.get(name) or synth.EXTRA_WORKLOADS[name]
             ost, og, ores = measure_workload(ow, dev, max(3, min(K, 20)), max(3, min(args.warmup, 5)),
                                              flush, stream, hbm, tflops)
             ores["roofline"]["peak_source"] = peak_kind
             ores["config"] = {"batch": ow.batch, "ctx_total": int(ost.lens_np.sum()),
-                              "ctx_max": int(ost.lens_np.max()), "mode": ow.mode}
+                              "ctx_max": int(ost.lens_np.max()), "mode": ow.mode,
+                              "new_tokens_per_seq": ow.q_len}
             others[name] = ores
             del ost, og
             torch.cuda.empty_cache()
@@ -554,7 +566,8 @@ def main():
 
 # measured beside the headline workload in the same run (the tiny fp32
 # workload is a parity case only)
-OTHER_WORKLOADS = ("dsv2_b4_ctx128k", "dsv2_b128_ragged", "dsv2_layer_b64_ctx32k")
+OTHER_WORKLOADS = ("dsv2_b4_ctx128k", "dsv2_b128_ragged", "dsv2_layer_b64_ctx32k",
+                   "dsv2_layer_b64_ctx32k_fused", "dsv2_b32_ctx4k_mtp2")
 
 
 if __name__ == "__main__":

@@ -170,6 +170,36 @@ mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* 
                            float* lse, mla_dtype dtype, const mla_dims* dims,
                            int32_t* dev_status, void* stream);
 
+/* (a5, several new tokens) Decode of q_len new tokens per sequence at once
+ * -- multi-token prediction and speculative drafts, DeepSeek-V2 MLA page 4.3
+ * and 6 (MLA combined with MTP). The q_len tokens of sequence b already sit
+ * at the last q_len of its seq_lens[b] cached positions (appended before
+ * the call), and new token t sees every cached position up to and
+ * including its own: seq_lens[b] - q_len + 1 + t of them. Query row
+ * v = b * q_len + t.
+ *   q_cat  [B][q_len][n_h][d_c + d_r]; o_lat [B][q_len][n_h][d_c] float;
+ *   lse    [B][q_len][n_h] float; the other arguments as for
+ *          mla_decode_attn, the workspace sized by
+ *          mla_decode_workspace_size(B * q_len, ...) and planned by
+ *          mla_plan_decode_mtp with the same seq_lens and q_len.
+ * Rows whose sequence the plan splits are finished by
+ * mla_combine(workspace, ws_bytes, B * q_len, ...); mla_absorb_q and
+ * mla_absorb_out take the B * q_len query rows as their batch.
+ * 1 <= q_len <= MLA_MAX_NEW_TOKENS; seq_lens[b] >= q_len (a shorter one is
+ * reported as MLA_DEV_BAD_LEN for the rows that would see no token). The
+ * query rows of one sequence sit next to each other in the plan, so the
+ * SMs that read the same pages run at about the same time and the second
+ * read of a page is served by L2. */
+#define MLA_MAX_NEW_TOKENS 8
+mla_status mla_plan_decode_mtp(const int32_t* seq_lens, int B, int q_len, int max_pages,
+                               void* workspace, size_t ws_bytes, mla_dtype dtype,
+                               const mla_dims* dims, int32_t* dev_status, void* stream);
+mla_status mla_decode_attn_mtp(const void* q_cat, const void* cache, const int32_t* block_table,
+                               int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                               int q_len, float softmax_scale, void* workspace, size_t ws_bytes,
+                               float* o_lat, float* lse, mla_dtype dtype, const mla_dims* dims,
+                               int32_t* dev_status, void* stream);
+
 /* (a6) Merge split partials: lse = log sum_s exp(lse_s),
  * o_lat = sum_s exp(lse_s - lse) o_s, for every sequence the plan split. */
 mla_status mla_combine(const void* workspace, size_t ws_bytes, int B, float* o_lat, float* lse,
@@ -199,6 +229,42 @@ mla_status mla_combine_absorb_out(const void* workspace, size_t ws_bytes, int B,
  *   u [B][d_model] float. fp32 accumulation. */
 mla_status mla_out_proj(const void* o, const void* w_o, float* u, int B, mla_dtype dtype,
                         const mla_dims* dims, void* stream);
+
+/* Fused absorption -- DeepSeek-V2 MLA page 2.2, the form that folds the
+ * up-projections into the neighbouring weights once, ahead of decoding:
+ * W~^Q = W^UQ^T W^UK (query side) and W~^O = W^O W^UV (output side). The
+ * per-head calls above (mla_absorb_q / mla_absorb_out) apply W^UK and W^UV
+ * unfused instead; these calls are the alternative, measured against it.
+ *
+ * mla_fuse_query_weights: w_uq_qr [n_h][d_h + d_r][K] (as for
+ *   mla_project_q, K = d_cq or d_model), w_uk [n_h*d_h][d_c] ->
+ *   w_fused_q [n_h][d_c + d_r][K]: per head the d_c rows of
+ *   W^UK_h^T W^UQ_h, then the d_r rows of W^QR_h unchanged. fp32
+ *   accumulation, one rounding to `dtype`.
+ * mla_project_q_absorbed: mla_project_q with w_fused_q in place of w_uq_qr:
+ *   writes q_cat [T][n_h][d_c + d_r] (RoPE on its last d_r columns)
+ *   directly, so no mla_absorb_q follows.
+ * mla_fuse_output_weights: w_o [d_model][n_h*d_v], w_uv [n_h*d_v][d_c] ->
+ *   w_fused_o [d_model][n_h*d_c] = the per-head products W^O_h W^UV_h side
+ *   by side. fp32 accumulation, one rounding to `dtype`.
+ * mla_out_proj_absorbed: u [B][d_model] float = w_fused_o . o_lat (o_lat
+ *   [B][n_h][d_c] float, flattened per row); for bf16 weights o_lat is first
+ *   rounded to bf16 into the caller's scratch o_lat_lowp [B][n_h*d_c]
+ *   (ignored for fp32). Replaces mla_absorb_out + mla_out_proj.
+ * The fused weights are larger: (d_c + d_r) K per head instead of
+ * (d_h + d_r) K + d_h d_c, and d_model n_h d_c instead of
+ * n_h d_v (d_model + d_c). */
+mla_status mla_fuse_query_weights(const void* w_uq_qr, const void* w_uk, void* w_fused_q,
+                                  mla_dtype dtype, const mla_dims* dims, void* stream);
+mla_status mla_project_q_absorbed(const void* x, const void* w_dq, const void* w_fused_q,
+                                  const int32_t* pos, int T, const float* rope, int max_pos,
+                                  void* c_q, void* q_cat, mla_dtype dtype, const mla_dims* dims,
+                                  int32_t* dev_status, void* stream);
+mla_status mla_fuse_output_weights(const void* w_o, const void* w_uv, void* w_fused_o,
+                                   mla_dtype dtype, const mla_dims* dims, void* stream);
+mla_status mla_out_proj_absorbed(const float* o_lat, void* o_lat_lowp, const void* w_fused_o,
+                                 float* u, int B, mla_dtype dtype, const mla_dims* dims,
+                                 void* stream);
 
 /* Allocation-free decode (the paper has no counterpart: this is a service
  * for callers, not a step of the method). Some callers cannot allocate

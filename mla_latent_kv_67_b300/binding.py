@@ -55,12 +55,19 @@ _SIGS = {
     "mla_decode_workspace_size": (_S, [_I, _I, _DIMS]),
     "mla_plan_decode": (_I, [_P, _I, _I, _P, _S, _I, _DIMS, _P, _P]),
     "mla_decode_attn": (_I, [_P, _P, _P, _I, _I, _P, _I, _F, _P, _S, _P, _P, _I, _DIMS, _P, _P]),
+    "mla_plan_decode_mtp": (_I, [_P, _I, _I, _I, _P, _S, _I, _DIMS, _P, _P]),
+    "mla_decode_attn_mtp": (_I, [_P, _P, _P, _I, _I, _P, _I, _I, _F, _P, _S, _P, _P, _I, _DIMS, _P,
+                                 _P]),
     "mla_combine": (_I, [_P, _S, _I, _P, _P, _I, _DIMS, _P]),
     "mla_decode_attn_static": (_I, [_P, _P, _P, _I, _I, _P, _I, _F, _P, _P, _I, _DIMS, _P, _P]),
     "mla_absorb_out": (_I, [_P, _P, _P, _I, _I, _I, _DIMS, _P]),
     "mla_combine_absorb_out": (_I, [_P, _S, _I, _P, _P, _P, _P, _I, _I, _DIMS, _P, _P]),
     "mla_tc_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "mla_out_proj": (_I, [_P, _P, _P, _I, _I, _DIMS, _P]),
+    "mla_fuse_query_weights": (_I, [_P, _P, _P, _I, _DIMS, _P]),
+    "mla_project_q_absorbed": (_I, [_P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _DIMS, _P, _P]),
+    "mla_fuse_output_weights": (_I, [_P, _P, _P, _I, _DIMS, _P]),
+    "mla_out_proj_absorbed": (_I, [_P, _P, _P, _P, _I, _I, _DIMS, _P]),
 }
 
 
@@ -215,6 +222,33 @@ def mla_decode_attn(q_cat, cache, block_table, seq_lens, scale: float, workspace
         _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
 
 
+def mla_plan_decode_mtp(seq_lens, q_len: int, max_pages: int, workspace, dtype: int, dims: Dims,
+                        dev_status=None, stream=None) -> None:
+    """Plan for q_len new tokens per sequence (query rows B * q_len)."""
+    B = seq_lens.shape[0]
+    _check(lib().mla_plan_decode_mtp(
+        _ptr(seq_lens, torch.int32, (B,), "seq_lens"), B, q_len, max_pages,
+        _ptr(workspace, torch.uint8, name="workspace"), workspace.numel(), dtype,
+        ctypes.byref(dims), _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
+
+
+def mla_decode_attn_mtp(q_cat, cache, block_table, seq_lens, q_len: int, scale: float, workspace,
+                        o_lat, lse, dims: Dims, dev_status=None, stream=None) -> None:
+    """Decode q_len new tokens per sequence; q_cat [B * q_len, n_h, d_c + d_r]."""
+    B, max_pages = block_table.shape
+    dt = _dt(cache)
+    R = B * q_len
+    _check(lib().mla_decode_attn_mtp(
+        _ptr(q_cat, cache.dtype, (R, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
+        _ptr(cache, shape=(cache.shape[0], dims.page_size, dims.d_c + dims.d_r), name="cache"),
+        _ptr(block_table, torch.int32, name="block_table"), max_pages, cache.shape[0],
+        _ptr(seq_lens, torch.int32, (B,), "seq_lens"), B, q_len, scale,
+        _ptr(workspace, torch.uint8, name="workspace"), workspace.numel(),
+        _ptr(o_lat, torch.float32, (R, dims.n_h, dims.d_c), "o_lat"),
+        _ptr(lse, torch.float32, (R, dims.n_h), "lse"), dt, ctypes.byref(dims),
+        _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
+
+
 def mla_combine(workspace, o_lat, lse, dtype: int, dims: Dims, stream=None) -> None:
     B = o_lat.shape[0]
     _check(lib().mla_combine(
@@ -267,3 +301,51 @@ def mla_decode_attn_static(q_cat, cache, block_table, seq_lens, scale: float, o_
         _ptr(o_lat, torch.float32, (B, dims.n_h, dims.d_c), "o_lat"),
         _ptr(lse, torch.float32, (B, dims.n_h), "lse"), dt, ctypes.byref(dims),
         _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
+
+
+# ------------------------------------------------------- fused absorption
+def mla_fuse_query_weights(w_uq_qr, w_uk, w_fused_q, dims: Dims, stream=None) -> None:
+    K = dims.d_cq or dims.d_model
+    dt = _dt(w_fused_q)
+    _check(lib().mla_fuse_query_weights(
+        _ptr(w_uq_qr, w_fused_q.dtype, (dims.n_h * (dims.d_h + dims.d_r), K), "w_uq_qr"),
+        _ptr(w_uk, w_fused_q.dtype, (dims.n_h * dims.d_h, dims.d_c), "w_uk"),
+        _ptr(w_fused_q, shape=(dims.n_h * (dims.d_c + dims.d_r), K), name="w_fused_q"), dt,
+        ctypes.byref(dims), _stream(stream)))
+
+
+def mla_project_q_absorbed(x, w_dq, w_fused_q, pos, rope, c_q, q_cat, dims: Dims,
+                           dev_status=None, stream=None) -> None:
+    dt = _dt(q_cat)
+    T = x.shape[0]
+    K = dims.d_cq or dims.d_model
+    _check(lib().mla_project_q_absorbed(
+        _ptr(x, q_cat.dtype, (T, dims.d_model), "x"),
+        _ptr(w_dq, q_cat.dtype, (dims.d_cq, dims.d_model), "w_dq") if dims.d_cq else None,
+        _ptr(w_fused_q, q_cat.dtype, (dims.n_h * (dims.d_c + dims.d_r), K), "w_fused_q"),
+        _ptr(pos, torch.int32, (T,), "pos"), T,
+        _ptr(rope, torch.float32, name="rope"), rope.shape[0] if rope is not None else 0,
+        _ptr(c_q, q_cat.dtype, (T, dims.d_cq), "c_q") if dims.d_cq else None,
+        _ptr(q_cat, shape=(T, dims.n_h, dims.d_c + dims.d_r), name="q_cat"), dt,
+        ctypes.byref(dims), _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
+
+
+def mla_fuse_output_weights(w_o, w_uv, w_fused_o, dims: Dims, stream=None) -> None:
+    dt = _dt(w_fused_o)
+    _check(lib().mla_fuse_output_weights(
+        _ptr(w_o, w_fused_o.dtype, (dims.d_model, dims.n_h * dims.d_v), "w_o"),
+        _ptr(w_uv, w_fused_o.dtype, (dims.n_h * dims.d_v, dims.d_c), "w_uv"),
+        _ptr(w_fused_o, shape=(dims.d_model, dims.n_h * dims.d_c), name="w_fused_o"), dt,
+        ctypes.byref(dims), _stream(stream)))
+
+
+def mla_out_proj_absorbed(o_lat, o_lat_lowp, w_fused_o, u, dims: Dims, stream=None) -> None:
+    B = o_lat.shape[0]
+    dt = _dt(w_fused_o)
+    _check(lib().mla_out_proj_absorbed(
+        _ptr(o_lat, torch.float32, (B, dims.n_h, dims.d_c), "o_lat"),
+        _ptr(o_lat_lowp, w_fused_o.dtype, (B, dims.n_h * dims.d_c), "o_lat_lowp")
+        if dt == MLA_BF16 else None,
+        _ptr(w_fused_o, shape=(dims.d_model, dims.n_h * dims.d_c), name="w_fused_o"),
+        _ptr(u, torch.float32, (B, dims.d_model), "u"), B, dt, ctypes.byref(dims),
+        _stream(stream)))

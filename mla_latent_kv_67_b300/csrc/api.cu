@@ -100,27 +100,31 @@ cudaError_t launch_decode(const DecodeSetup& ds, const void* q_cat, const void* 
                           const int32_t* block_table, int max_pages, int num_pages, int B,
                           float softmax_scale, void* ws, float* o_lat, float* lse, mla_dtype dtype,
                           const mla_dims* d, int32_t* dev_status, cudaStream_t s) {
+  const int rows = B * ds.q_len;  // query rows
   if (ds.path == 1)
-    return tc_split_launch(q_cat, cache, block_table, max_pages, num_pages, B, ds.workers,
-                           softmax_scale, ws, ds.L, o_lat, lse, dev_status, s);
+    return tc_split_launch(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
+                           softmax_scale, ws, ds.L, o_lat, lse, dev_status, ds.q_len, s);
   if (ds.path == 2)
-    return tc_pair_launch(q_cat, cache, block_table, max_pages, num_pages, B, ds.workers,
-                          softmax_scale, ws, ds.L, o_lat, lse, dev_status, s);
-  return launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, B, ds.workers,
+    return tc_pair_launch(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
+                          softmax_scale, ws, ds.L, o_lat, lse, dev_status, ds.q_len, s);
+  return launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
                             softmax_scale, ws, ds.L, o_lat, lse, d->n_h, d->d_c, d->d_r,
-                            d->page_size, dtype == MLA_F32, dev_status, s);
+                            d->page_size, dtype == MLA_F32, dev_status, ds.q_len, s);
 }
 
 mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* block_table,
-                        int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                        int max_pages, int num_pages, const int32_t* seq_lens, int B, int q_len,
                         const float* o_lat, const float* lse, mla_dtype dtype,
                         const mla_dims* dims, DecodeSetup* out) {
   mla_status st = check_dims(dims);
   if (st != MLA_OK) return st;
   if ((st = check_dtype(dtype)) != MLA_OK) return st;
   REQUIRE(B >= 0, "B must be >= 0");
+  REQUIRE(q_len >= 1 && q_len <= MLA_MAX_NEW_TOKENS, "q_len must be in [1, %d] (got %d)",
+          MLA_MAX_NEW_TOKENS, q_len);
   out->path = 0;
   out->workers = 0;
+  out->q_len = q_len;
   if (B == 0) return MLA_OK;
   REQUIRE(q_cat && cache && block_table && seq_lens && o_lat && lse, "NULL tensor argument");
   REQUIRE(max_pages > 0 && num_pages > 0, "max_pages and num_pages must be > 0");
@@ -128,7 +132,7 @@ mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* blo
   out->path = pick_path(dtype, dims);
   out->workers = workers_for(out->path);
   if (out->workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
-  out->L = workspace_layout(B, out->workers, dims->n_h, dims->d_c);
+  out->L = workspace_layout(B * q_len, out->workers, dims->n_h, dims->d_c);
   return MLA_OK;
 }
 }  // namespace mla
@@ -204,16 +208,23 @@ mla_status mla_append_latent(const void* x, const void* w_dkv_kr, const int32_t*
   return cuda_status(projection(g, S(stream)), "append_latent");
 }
 
-mla_status mla_project_q(const void* x, const void* w_dq, const void* w_uq_qr,
-                         const int32_t* pos, int T, const float* rope, int max_pos,
-                         void* c_q, void* q, mla_dtype dtype, const mla_dims* dims,
+}  // extern "C"
+
+namespace {
+// c_Q = x W^DQ^T (or x), then per head [W_up_h] c_Q with RoPE on the last
+// d_r of every `per_head` output columns: the query projection (per_head =
+// d_h + d_r) or, with the fused W^UK^T W^UQ rows, q_cat itself (per_head =
+// d_c + d_r).
+mla_status project_query(const void* x, const void* w_dq, const void* w_up, const int32_t* pos,
+                         int T, const float* rope, int max_pos, void* c_q, void* out,
+                         mla_dtype dtype, const mla_dims* dims, int per_head, int rope_off,
                          int32_t* dev_status, void* stream) {
   mla_status st = check_dims(dims);
   if (st != MLA_OK) return st;
   if ((st = check_dtype(dtype)) != MLA_OK) return st;
   REQUIRE(T >= 0, "T must be >= 0");
   if (T == 0) return MLA_OK;
-  REQUIRE(x && w_uq_qr && pos && q, "NULL tensor argument");
+  REQUIRE(x && w_up && pos && out, "NULL tensor argument");
   REQUIRE(dims->d_model > 0, "project_q needs d_model > 0");
   REQUIRE(dims->d_cq == 0 || (w_dq && c_q), "d_cq > 0 needs w_dq and the c_q scratch");
   REQUIRE(dims->d_r == 0 || (rope && max_pos > 0), "RoPE table required when d_r > 0");
@@ -230,15 +241,110 @@ mla_status mla_project_q(const void* x, const void* w_dq, const void* w_uq_qr,
     src = c_q;
     K = dims->d_cq;
   }
-  const int per_head = dims->d_h + dims->d_r;
   GemmArgs g = {};
   g.a = src; g.a_ms = K; g.a_f32 = f32;
-  g.w = w_uq_qr; g.w_ns = K; g.w_ks = 1; g.w_f32 = f32;
+  g.w = w_up; g.w_ns = K; g.w_ks = 1; g.w_f32 = f32;
   g.G = 1; g.M = T; g.N = dims->n_h * per_head; g.K = K;
-  g.epi = EPI_ROPE; g.out = q; g.o_ms = g.N; g.o_f32 = f32;
-  g.rope = rope; g.max_pos = max_pos; g.d_r = dims->d_r; g.rope_off = dims->d_h;
+  g.epi = EPI_ROPE; g.out = out; g.o_ms = g.N; g.o_f32 = f32;
+  g.rope = rope; g.max_pos = max_pos; g.d_r = dims->d_r; g.rope_off = rope_off;
   g.rope_period = per_head; g.pos = pos; g.dev_status = dev_status;
-  return cuda_status(projection(g, S(stream)), "project_q/W^UQ|W^QR");
+  return cuda_status(projection(g, S(stream)), "project_q/up-projection");
+}
+}  // namespace
+
+extern "C" {
+
+mla_status mla_project_q(const void* x, const void* w_dq, const void* w_uq_qr,
+                         const int32_t* pos, int T, const float* rope, int max_pos,
+                         void* c_q, void* q, mla_dtype dtype, const mla_dims* dims,
+                         int32_t* dev_status, void* stream) {
+  if (!dims) return fail(MLA_ERR_INVALID_ARG, "dims is NULL");
+  return project_query(x, w_dq, w_uq_qr, pos, T, rope, max_pos, c_q, q, dtype, dims,
+                       dims->d_h + dims->d_r, dims->d_h, dev_status, stream);
+}
+
+mla_status mla_fuse_query_weights(const void* w_uq_qr, const void* w_uk, void* w_fused_q,
+                                  mla_dtype dtype, const mla_dims* dims, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(w_uq_qr && w_uk && w_fused_q, "NULL tensor argument");
+  REQUIRE(dims->d_model > 0, "fusing the query weights needs d_model > 0");
+  const int f32 = dtype == MLA_F32;
+  const int K = dims->d_cq > 0 ? dims->d_cq : dims->d_model;
+  const long long in_h = (long long)(dims->d_h + dims->d_r) * K;   // one head of w_uq_qr
+  const long long out_h = (long long)(dims->d_c + dims->d_r) * K;  // one head of w_fused_q
+  // F_h[c][j] = sum_i W^UK[h d_h + i][c] W^UQ_h[i][j]
+  GemmArgs g = {};
+  g.a = w_uk; g.a_gs = (long long)dims->d_h * dims->d_c; g.a_ms = 1; g.a_ks = dims->d_c;
+  g.a_f32 = f32;
+  g.w = w_uq_qr; g.w_gs = in_h; g.w_ns = 1; g.w_ks = K; g.w_f32 = f32;
+  g.G = dims->n_h; g.M = dims->d_c; g.N = K; g.K = dims->d_h;
+  g.epi = EPI_STORE; g.out = w_fused_q; g.o_gs = out_h; g.o_ms = K; g.o_f32 = f32;
+  if ((st = cuda_status(launch_simt_gemm(g, S(stream)), "fuse_query_weights")) != MLA_OK) return st;
+  // the W^QR rows of every head follow unchanged
+  const int esz = f32 ? 4 : 2;
+  const char* src = reinterpret_cast<const char*>(w_uq_qr) + (size_t)dims->d_h * K * esz;
+  char* dst = reinterpret_cast<char*>(w_fused_q) + (size_t)dims->d_c * K * esz;
+  return cuda_status(launch_copy_rows(src, in_h, K, dst, out_h, K, dims->n_h, dims->d_r, K, esz,
+                                      S(stream)),
+                     "fuse_query_weights/W^QR");
+}
+
+mla_status mla_project_q_absorbed(const void* x, const void* w_dq, const void* w_fused_q,
+                                  const int32_t* pos, int T, const float* rope, int max_pos,
+                                  void* c_q, void* q_cat, mla_dtype dtype, const mla_dims* dims,
+                                  int32_t* dev_status, void* stream) {
+  if (!dims) return fail(MLA_ERR_INVALID_ARG, "dims is NULL");
+  return project_query(x, w_dq, w_fused_q, pos, T, rope, max_pos, c_q, q_cat, dtype, dims,
+                       dims->d_c + dims->d_r, dims->d_c, dev_status, stream);
+}
+
+mla_status mla_fuse_output_weights(const void* w_o, const void* w_uv, void* w_fused_o,
+                                   mla_dtype dtype, const mla_dims* dims, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(w_o && w_uv && w_fused_o, "NULL tensor argument");
+  REQUIRE(dims->d_model > 0, "fusing the output weights needs d_model > 0");
+  const int f32 = dtype == MLA_F32;
+  // F^O[n][h d_c + c] = sum_v W^O[n][h d_v + v] W^UV[h d_v + v][c]
+  GemmArgs g = {};
+  g.a = w_o; g.a_gs = dims->d_v; g.a_ms = (long long)dims->n_h * dims->d_v; g.a_ks = 1;
+  g.a_f32 = f32;
+  g.w = w_uv; g.w_gs = (long long)dims->d_v * dims->d_c; g.w_ns = 1; g.w_ks = dims->d_c;
+  g.w_f32 = f32;
+  g.G = dims->n_h; g.M = dims->d_model; g.N = dims->d_c; g.K = dims->d_v;
+  g.epi = EPI_STORE; g.out = w_fused_o; g.o_gs = dims->d_c;
+  g.o_ms = (long long)dims->n_h * dims->d_c; g.o_f32 = f32;
+  return cuda_status(launch_simt_gemm(g, S(stream)), "fuse_output_weights");
+}
+
+mla_status mla_out_proj_absorbed(const float* o_lat, void* o_lat_lowp, const void* w_fused_o,
+                                 float* u, int B, mla_dtype dtype, const mla_dims* dims,
+                                 void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(B >= 0, "B must be >= 0");
+  if (B == 0) return MLA_OK;
+  REQUIRE(o_lat && w_fused_o && u, "NULL tensor argument");
+  REQUIRE(dims->d_model > 0, "out_proj needs d_model > 0");
+  const int K = dims->n_h * dims->d_c;
+  const void* a = o_lat;
+  if (dtype == MLA_BF16) {
+    REQUIRE(o_lat_lowp != nullptr, "bf16 weights need the o_lat_lowp scratch");
+    if ((st = cuda_status(launch_to_bf16(o_lat, o_lat_lowp, (long long)B * K, S(stream)),
+                          "out_proj_absorbed/round")) != MLA_OK)
+      return st;
+    a = o_lat_lowp;
+  }
+  GemmArgs g = {};
+  g.a = a; g.a_ms = K; g.a_f32 = dtype == MLA_F32;
+  g.w = w_fused_o; g.w_ns = K; g.w_ks = 1; g.w_f32 = dtype == MLA_F32;
+  g.G = 1; g.M = B; g.N = dims->d_model; g.K = K;
+  g.epi = EPI_STORE; g.out = u; g.o_ms = dims->d_model; g.o_f32 = 1;
+  return cuda_status(projection(g, S(stream)), "out_proj_absorbed");
 }
 
 mla_status mla_absorb_q(const void* q, const void* w_uk, void* q_cat, int B, mla_dtype dtype,
@@ -274,33 +380,42 @@ size_t mla_decode_workspace_size(int B, mla_dtype dtype, const mla_dims* dims) {
   return workspace_layout(B, workers, dims->n_h, dims->d_c).total;
 }
 
-mla_status mla_plan_decode(const int32_t* seq_lens, int B, int max_pages, void* workspace,
-                           size_t ws_bytes, mla_dtype dtype, const mla_dims* dims,
-                           int32_t* dev_status, void* stream) {
+mla_status mla_plan_decode_mtp(const int32_t* seq_lens, int B, int q_len, int max_pages,
+                               void* workspace, size_t ws_bytes, mla_dtype dtype,
+                               const mla_dims* dims, int32_t* dev_status, void* stream) {
   mla_status st = check_dims(dims);
   if (st != MLA_OK) return st;
   if ((st = check_dtype(dtype)) != MLA_OK) return st;
   REQUIRE(B >= 0 && max_pages > 0, "B must be >= 0 and max_pages > 0");
+  REQUIRE(q_len >= 1 && q_len <= MLA_MAX_NEW_TOKENS, "q_len must be in [1, %d] (got %d)",
+          MLA_MAX_NEW_TOKENS, q_len);
   if (B == 0) return MLA_OK;
   REQUIRE(seq_lens != nullptr, "seq_lens is NULL");
   const int path = pick_path(dtype, dims);
   const int workers = workers_for(path);
   if (workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
-  const WorkspaceLayout L = workspace_layout(B, workers, dims->n_h, dims->d_c);
+  const WorkspaceLayout L = workspace_layout(B * q_len, workers, dims->n_h, dims->d_c);
   if (!workspace || ws_bytes < L.total)
     return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L.total);
-  return cuda_status(launch_plan(seq_lens, B, max_pages, dims->page_size, workers, path,
+  return cuda_status(launch_plan(seq_lens, B, q_len, max_pages, dims->page_size, workers, path,
                                  workspace, L, dev_status, S(stream)),
                      "plan_decode");
 }
 
-mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* block_table,
-                           int max_pages, int num_pages, const int32_t* seq_lens, int B,
-                           float softmax_scale, void* workspace, size_t ws_bytes, float* o_lat,
-                           float* lse, mla_dtype dtype, const mla_dims* dims,
+mla_status mla_plan_decode(const int32_t* seq_lens, int B, int max_pages, void* workspace,
+                           size_t ws_bytes, mla_dtype dtype, const mla_dims* dims,
                            int32_t* dev_status, void* stream) {
+  return mla_plan_decode_mtp(seq_lens, B, 1, max_pages, workspace, ws_bytes, dtype, dims,
+                             dev_status, stream);
+}
+
+mla_status mla_decode_attn_mtp(const void* q_cat, const void* cache, const int32_t* block_table,
+                               int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                               int q_len, float softmax_scale, void* workspace, size_t ws_bytes,
+                               float* o_lat, float* lse, mla_dtype dtype, const mla_dims* dims,
+                               int32_t* dev_status, void* stream) {
   DecodeSetup ds;
-  mla_status st = decode_setup(q_cat, cache, block_table, max_pages, num_pages, seq_lens, B,
+  mla_status st = decode_setup(q_cat, cache, block_table, max_pages, num_pages, seq_lens, B, q_len,
                                o_lat, lse, dtype, dims, &ds);
   if (st != MLA_OK || B == 0) return st;
   if (!workspace || ws_bytes < ds.L.total)
@@ -310,6 +425,16 @@ mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* 
                                    softmax_scale, workspace, o_lat, lse, dtype, dims, dev_status,
                                    S(stream)),
                      ds.path == 0 ? "decode_attn (simt)" : "decode_attn (tcgen05)");
+}
+
+mla_status mla_decode_attn(const void* q_cat, const void* cache, const int32_t* block_table,
+                           int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                           float softmax_scale, void* workspace, size_t ws_bytes, float* o_lat,
+                           float* lse, mla_dtype dtype, const mla_dims* dims,
+                           int32_t* dev_status, void* stream) {
+  return mla_decode_attn_mtp(q_cat, cache, block_table, max_pages, num_pages, seq_lens, B, 1,
+                             softmax_scale, workspace, ws_bytes, o_lat, lse, dtype, dims,
+                             dev_status, stream);
 }
 
 mla_status mla_combine(const void* workspace, size_t ws_bytes, int B, float* o_lat, float* lse,

@@ -10,7 +10,7 @@ namespace mla {
 
 // Generic CUDA-core batched GEMM with fused epilogues:
 //   out[g][m][n] = sum_k A[g][m][k] * W[g](n, k)
-// A element (g,m,k) at a + g*a_gs + m*a_ms + k;
+// A element (g,m,k) at a + g*a_gs + m*a_ms + k*a_ks (a_ks == 0 means 1);
 // W element (g,n,k) at w + g*w_gs + n*w_ns + k*w_ks.
 enum Epilogue {
   EPI_STORE = 0,   // out + g*o_gs + m*o_ms + n
@@ -19,7 +19,7 @@ enum Epilogue {
 };
 
 struct GemmArgs {
-  const void* a; long long a_gs, a_ms; int a_f32;
+  const void* a; long long a_gs, a_ms; int a_f32; long long a_ks;
   const void* w; long long w_gs, w_ns, w_ks; int w_f32;
   int G, M, N, K;
   int epi;
@@ -41,16 +41,28 @@ cudaError_t tc_gemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s);
 cudaError_t launch_copy_rope_part(const void* q, void* q_cat, int B, int n_h, int d_h, int d_r,
                                   int d_c, int f32, cudaStream_t s);
 cudaError_t launch_rope_table(float* cs, int max_pos, int d_r, double base, cudaStream_t s);
+// dst[g][r][j] = src[g][r][j] for r < rows, j < cols (bf16 or fp32 elements of
+// `esz` bytes); row strides in elements, group strides in elements.
+cudaError_t launch_copy_rows(const void* src, long long src_gs, long long src_rs, void* dst,
+                             long long dst_gs, long long dst_rs, int G, int rows, int cols,
+                             int esz, cudaStream_t s);
+// dst[i] = bf16(src[i]) for i < n.
+cudaError_t launch_to_bf16(const float* src, void* dst, long long n, cudaStream_t s);
 
+// Decode launchers take B = the number of query rows (sequences x new
+// tokens per sequence) and bt_div = new tokens per sequence: query row s
+// reads block-table row s / bt_div.
 cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32_t* block_table,
                                int max_pages, int num_pages, int B, int workers, float scale,
                                const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
                                int n_h, int d_c, int d_r, int page_size, int f32,
-                               int32_t* dev_status, cudaStream_t s);
+                               int32_t* dev_status, int bt_div, cudaStream_t s);
 
-cudaError_t launch_plan(const int32_t* seq_lens, int B, int max_pages, int page_size, int workers,
-                        int path, void* ws, const WorkspaceLayout& L, int32_t* dev_status,
-                        cudaStream_t s);
+// Plan for B sequences with q_len new tokens each: B * q_len query rows;
+// row v = b * q_len + t sees seq_lens[b] - (q_len - 1 - t) cached tokens.
+cudaError_t launch_plan(const int32_t* seq_lens, int B, int q_len, int max_pages, int page_size,
+                        int workers, int path, void* ws, const WorkspaceLayout& L,
+                        int32_t* dev_status, cudaStream_t s);
 cudaError_t launch_combine(const void* ws, const WorkspaceLayout& L, int B, int n_h, int d_c,
                            float* o_lat, float* lse, cudaStream_t s);
 
@@ -63,13 +75,14 @@ int pick_path(mla_dtype dt, const mla_dims* d);  // 1 tcgen05, 0 SIMT
 int workers_for(int path);                       // workers the plan cuts the pages into
 struct DecodeSetup {
   int path, workers;
+  int q_len;        // new tokens per sequence (query rows = B * q_len)
   WorkspaceLayout L;
 };
 // Validates the arguments of a decode call exactly as mla_decode_attn does
 // and picks its kernel, worker count and workspace layout. B == 0 is valid
 // (nothing to do; `out` then has workers == 0).
 mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* block_table,
-                        int max_pages, int num_pages, const int32_t* seq_lens, int B,
+                        int max_pages, int num_pages, const int32_t* seq_lens, int B, int q_len,
                         const float* o_lat, const float* lse, mla_dtype dtype,
                         const mla_dims* dims, DecodeSetup* out);
 // The decode kernel `ds` selects, on workspace `ws` (planned by launch_plan).

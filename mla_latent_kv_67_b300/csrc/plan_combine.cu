@@ -44,7 +44,8 @@ constexpr int PLAN_SMEM_SEQS = 4096;  // sequences whose cost prefix stays in sh
 // and worker g takes the pages whose units fall in its range: a worker that
 // starts a sequence inside its range gets c_seg pages fewer.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens, int B,
-                                                    int max_pages, int page_size, int workers,
+                                                    int q_len, int max_pages, int page_size,
+                                                    int workers,
                                                     int path, int c_seg, char* ws, WorkspaceLayout L,
                                                     int32_t* dev_status) {
   __shared__ int warp_sums[32];
@@ -63,7 +64,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     const int b = base + threadIdx.x;
     int pages = 0, len = 0;
     if (b < B) {
-      len = seq_lens[b];
+      // query row b is new token b % q_len of sequence b / q_len
+      len = seq_lens[b / q_len] - (q_len - 1 - b % q_len);
       if (len < 1 || (long long)len > (long long)max_pages * page_size) {
         report(dev_status, MLA_DEV_BAD_LEN);
         len = 0;
@@ -260,14 +262,14 @@ __global__ void __launch_bounds__(128) combine_kernel(const char* __restrict__ w
   if (lane == 0) lse[(size_t)b * n_h + h] = m + logf(z);
 }
 
-cudaError_t launch_plan(const int32_t* seq_lens, int B, int max_pages, int page_size, int workers,
-                        int path, void* ws, const WorkspaceLayout& L, int32_t* dev_status,
-                        cudaStream_t s) {
+cudaError_t launch_plan(const int32_t* seq_lens, int B, int q_len, int max_pages, int page_size,
+                        int workers, int path, void* ws, const WorkspaceLayout& L,
+                        int32_t* dev_status, cudaStream_t s) {
   // the tcgen05 kernel's per-sequence cost (Q fetch, O write-out) is worth
   // about four pages; the SIMT kernel's is small next to its page cost
   const int c_seg = path >= 1 ? 4 : 0;
-  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, B, max_pages, page_size, workers, path, c_seg, (char*)ws,
-                                 L, dev_status);
+  plan_kernel<<<1, 1024, 0, s>>>(seq_lens, B * q_len, q_len, max_pages, page_size, workers, path,
+                                 c_seg, (char*)ws, L, dev_status);
   return cudaGetLastError();
 }
 

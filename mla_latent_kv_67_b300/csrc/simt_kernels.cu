@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(GemmArgs p) {
   const int m0 = blockIdx.y * GB_M, n0 = blockIdx.x * GB_N;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const long long a_base = (long long)g * p.a_gs;
+  const long long a_ks = p.a_ks ? p.a_ks : 1;
   const long long w_base = (long long)g * p.w_gs;
   const bool w_kmajor = p.w_ks == 1;
   float acc[4][2] = {};
@@ -57,7 +58,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(GemmArgs p) {
     for (int idx = threadIdx.x; idx < GB_M * GB_K; idx += 256) {
       const int mm = idx / GB_K, kk = idx % GB_K;
       const int m = m0 + mm, k = k0 + kk;
-      As[mm][kk] = (m < p.M && k < p.K) ? ld_any(p.a, a_base + m * p.a_ms + k, p.a_f32) : 0.f;
+      As[mm][kk] = (m < p.M && k < p.K) ? ld_any(p.a, a_base + m * p.a_ms + k * a_ks, p.a_f32) : 0.f;
     }
     for (int idx = threadIdx.x; idx < GB_N * GB_K; idx += 256) {
       int nn, kk;
@@ -135,6 +136,49 @@ cudaError_t launch_simt_gemm(const GemmArgs& g, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+__global__ void copy_rows_kernel(const char* src, long long src_gs, long long src_rs, char* dst,
+                                 long long dst_gs, long long dst_rs, int rows, int cols, int esz) {
+  const int g = blockIdx.y;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)rows * cols;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / cols, j = i % cols;
+    const char* a = src + (g * src_gs + r * src_rs + j) * esz;
+    char* b = dst + (g * dst_gs + r * dst_rs + j) * esz;
+    if (esz == 4) *reinterpret_cast<float*>(b) = *reinterpret_cast<const float*>(a);
+    else *reinterpret_cast<__nv_bfloat16*>(b) = *reinterpret_cast<const __nv_bfloat16*>(a);
+  }
+}
+
+cudaError_t launch_copy_rows(const void* src, long long src_gs, long long src_rs, void* dst,
+                             long long dst_gs, long long dst_rs, int G, int rows, int cols,
+                             int esz, cudaStream_t s) {
+  if (G == 0 || rows == 0 || cols == 0) return cudaSuccess;
+  const long long n = (long long)rows * cols;
+  const int blocks = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+  copy_rows_kernel<<<dim3(blocks, G), 256, 0, s>>>((const char*)src, src_gs, src_rs, (char*)dst,
+                                                   dst_gs, dst_rs, rows, cols, esz);
+  return cudaGetLastError();
+}
+
+__global__ void to_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, long long n4) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = src[i];
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    dst[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+}
+
+cudaError_t launch_to_bf16(const float* src, void* dst, long long n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  if (n % 4 != 0) return cudaErrorInvalidValue;
+  const long long n4 = n / 4;
+  const int blocks = (int)((n4 + 255) / 256 < 2048 ? (n4 + 255) / 256 : 2048);
+  to_bf16_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(src),
+                                         reinterpret_cast<uint2*>(dst), n4);
+  return cudaGetLastError();
+}
+
 // q_cat[b][h][d_c + r] = q[b][h][d_h + r]
 __global__ void copy_rope_part_kernel(const void* q, void* q_cat, int B, int n_h, int d_h, int d_r,
                                       int d_c, int f32) {
@@ -168,7 +212,7 @@ __global__ void __launch_bounds__(256) simt_decode_kernel(
     const T* __restrict__ q_cat, const T* __restrict__ cache, const int32_t* __restrict__ block_table,
     int max_pages, int num_pages, int B, float scale, const char* __restrict__ ws, WorkspaceLayout L,
     float* __restrict__ o_lat, float* __restrict__ lse_out, int n_h, int d_c, int d_r,
-    int page_size, int32_t* dev_status) {
+    int page_size, int32_t* dev_status, int bt_div) {
   extern __shared__ float smem[];
   const int W = d_c + d_r, Wp = W + 1;
   float* tile = smem;                     // [SD_TOK][Wp]
@@ -207,7 +251,7 @@ __global__ void __launch_bounds__(256) simt_decode_kernel(
         long long off = -1;
         if ((int)threadIdx.x < nt) {
           const int tok = t0 + threadIdx.x;
-          const int blk = block_table[(size_t)s * max_pages + tok / page_size];
+          const int blk = block_table[(size_t)(s / bt_div) * max_pages + tok / page_size];
           if (blk < 0 || blk >= num_pages) report(dev_status, MLA_DEV_BAD_BLOCK);
           else off = ((long long)blk * page_size + tok % page_size) * W;
         }
@@ -273,7 +317,7 @@ cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32
                                int max_pages, int num_pages, int B, int workers, float scale,
                                const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
                                int n_h, int d_c, int d_r, int page_size, int f32,
-                               int32_t* dev_status, cudaStream_t s) {
+                               int32_t* dev_status, int bt_div, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   const int W = d_c + d_r;
   const size_t smem = sizeof(float) * ((size_t)SD_TOK * (W + 1) + (size_t)SD_HEADS * W);
@@ -284,13 +328,13 @@ cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32
     if (e != cudaSuccess) return e;
     simt_decode_kernel<float><<<grid, 256, smem, s>>>(
         (const float*)q_cat, (const float*)cache, block_table, max_pages, num_pages, B, scale,
-        (const char*)ws, L, o_lat, lse, n_h, d_c, d_r, page_size, dev_status);
+        (const char*)ws, L, o_lat, lse, n_h, d_c, d_r, page_size, dev_status, bt_div);
   } else {
     e = cudaFuncSetAttribute(simt_decode_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     simt_decode_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(
         (const __nv_bfloat16*)q_cat, (const __nv_bfloat16*)cache, block_table, max_pages, num_pages,
-        B, scale, (const char*)ws, L, o_lat, lse, n_h, d_c, d_r, page_size, dev_status);
+        B, scale, (const char*)ws, L, o_lat, lse, n_h, d_c, d_r, page_size, dev_status, bt_div);
   }
   return cudaGetLastError();
 }

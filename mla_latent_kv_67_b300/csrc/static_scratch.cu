@@ -66,7 +66,7 @@ extern "C" mla_status mla_decode_attn_static(const void* q_cat, const void* cach
   using namespace mla;
   // the same checks, kernel choice and plan layout as mla_decode_attn
   DecodeSetup ds;
-  mla_status st = decode_setup(q_cat, cache, block_table, max_pages, num_pages, seq_lens, B,
+  mla_status st = decode_setup(q_cat, cache, block_table, max_pages, num_pages, seq_lens, B, 1,
                                o_lat, lse, dtype, d, &ds);
   if (st != MLA_OK || B == 0) return st;
   if (ds.L.total > (size_t)MLA_STATIC_SCRATCH_BYTES)
@@ -82,8 +82,8 @@ extern "C" mla_status mla_decode_attn_static(const void* q_cat, const void* cach
   // Nothing in the scratch needs to start at zero: the plan kernel rewrites
   // every plan entry it reads back, and each partial slot is written by the
   // decode kernel before the combine kernel reads it.
-  e = launch_plan(seq_lens, B, max_pages, d->page_size, ds.workers, ds.path, ws, ds.L, dev_status,
-                  s);
+  e = launch_plan(seq_lens, B, 1, max_pages, d->page_size, ds.workers, ds.path, ws, ds.L,
+                  dev_status, s);
   if (e == cudaSuccess)
     e = launch_decode(ds, q_cat, cache, block_table, max_pages, num_pages, B, softmax_scale, ws,
                       o_lat, lse, dtype, d, dev_status, s);

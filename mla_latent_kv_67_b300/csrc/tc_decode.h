@@ -16,13 +16,13 @@ int tc_split_workers(int sms);
 cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t* block_table,
                             int max_pages, int num_pages, int B, int workers, float scale,
                             const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
-                            int32_t* dev_status, cudaStream_t s);
+                            int32_t* dev_status, int bt_div, cudaStream_t s);
 // The score/value pair kernel (score CTA + value CTA per worker).
 int tc_pair_workers(int sms);
 cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* block_table,
                            int max_pages, int num_pages, int B, int workers, float scale,
                            const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
-                           int32_t* dev_status, cudaStream_t s);
+                           int32_t* dev_status, int bt_div, cudaStream_t s);
 
 // tcgen05 absorption products (DeepSeek-V2 shapes, bf16 weights).
 bool tc_absorb_supported(int n_h, int d_h, int d_r, int d_c, int d_v);

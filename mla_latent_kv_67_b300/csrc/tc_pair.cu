@@ -152,6 +152,7 @@ struct Params {
   int32_t* dev_status;
   int max_pages, num_pages;
   float scale_log2;
+  int bt_div;  // new tokens per sequence: query row s uses block-table row s / bt_div
 };
 
 // A sequence's share of a worker's page range.
@@ -225,7 +226,7 @@ __device__ __forceinline__ bool for_each_page(const Params& p, const WorkerPlan&
     for (int pb = sg.p0; ok && pb < sg.p1; pb += 32) {
       int blk = 0;
       if (pb + lane < sg.p1) {
-        blk = p.block_table[(size_t)s * p.max_pages + pb + lane];
+        blk = p.block_table[(size_t)(s / p.bt_div) * p.max_pages + pb + lane];
         if (blk < 0 || blk >= p.num_pages) {
           report(p.dev_status, MLA_DEV_BAD_BLOCK);
           blk = 0;
@@ -843,7 +844,7 @@ int tc_pair_workers(int sms) {
 cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* block_table,
                            int max_pages, int num_pages, int B, int workers, float scale,
                            const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
-                           int32_t* dev_status, cudaStream_t s) {
+                           int32_t* dev_status, int bt_div, cudaStream_t s) {
   CUtensorMap tm_cache, tm_q;
   cudaError_t e = tcp::make_cache_map(&tm_cache, cache, (uint64_t)num_pages * tcp::PAGE);
   if (e != cudaSuccess) return e;
@@ -860,6 +861,7 @@ cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* 
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.bt_div = bt_div > 0 ? bt_div : 1;
   static unsigned long long smem_done = 0;
   e = set_max_smem_once((const void*)tcp::tc_pair_decode_kernel, (int)tcp::SMEM_BYTES, smem_done);
   if (e != cudaSuccess) return e;

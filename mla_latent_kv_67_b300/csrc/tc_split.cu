@@ -14,10 +14,11 @@
 // owns the 64 RoPE columns. Each CTA reads only its columns of a page
 // (40 KB / 32 KB instead of the whole 72 KB row block), computes the partial
 // score S_r over its columns, and the two partials are exchanged through
-// distributed shared memory (st.async, completion counted in bytes on the
-// receiver's barrier): both CTAs then hold S = S_0 + S_1, bit for bit the
-// same, and run the same online softmax, so each can multiply the
-// probabilities into its own half of O. At a sequence's end each CTA writes
+// distributed shared memory (each CTA stores its partial in its own shared
+// memory and loads the peer's; two barriers per page with one remote
+// arrival per row synchronise the pair): both CTAs then hold
+// S = S_0 + S_1, bit for bit the same, and run the same online softmax, so
+// each can multiply the probabilities into its own half of O. At a sequence's end each CTA writes
 // its own 128 KB of O, so the write-out of a split partial takes half as
 // long as from one SM.
 //
@@ -75,8 +76,8 @@ enum {
   QFULL = PFREE + 2,     // Q latent half of the sequence landed
   QFREE = QFULL + 1,     // last S of the sequence done (commit)
   QRREADY = QFREE + 1,   // RoPE query in TMEM (4 warps; rank 0)
-  XFULL = QRREADY + 1,   // the peer's partial S landed (4 arms + bytes)
-  XFREE = XFULL + 1,     // the peer consumed our partial S (4 remote arrivals)
+  XREADY = QRREADY + 1,  // the peer's partial S is in its buffer (128 remote arrivals)
+  XFREE = XREADY + 1,    // the peer has read our partial S (128 remote arrivals)
   LREADY = XFREE + 1,    // [2] 1 / l of a sequence written (4 softmax warps)
   LFREE = LREADY + 2,    // [2] 1 / l read by the 4 epilogue warps
   ODONE = LFREE + 2,     // last PV of a sequence done (commit)
@@ -116,6 +117,7 @@ struct Params {
   int32_t* dev_status;
   int max_pages, num_pages;
   float scale_log2;
+  int bt_div;    // new tokens per sequence: query row s uses block-table row s / bt_div
   int withhold;  // read by the test build only: the page producer issues nothing
 };
 
@@ -192,12 +194,20 @@ __device__ __forceinline__ uint4 ldg_nc_u4(const uint4* p) {
                : "l"(p));
   return v;
 }
-// 16-byte shared-memory load at a 32-bit shared address.
-__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+// 16-byte store to this CTA's shared memory.
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+// 16-byte load from another CTA's shared memory (cluster address from mapa).
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
   uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
   return v;
 }
 // 32-byte global store.
@@ -244,8 +254,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(cx.bar(QFULL), 1);
     mbar_init(cx.bar(QFREE), 1);
     mbar_init(cx.bar(QRREADY), 4);
-    mbar_init(cx.bar(XFULL), 4);
-    mbar_init(cx.bar(XFREE), 4);
+    mbar_init(cx.bar(XREADY), NH);
+    mbar_init(cx.bar(XFREE), NH);
     mbar_init(cx.bar(ODONE), 1);
     mbar_init(cx.bar(OFREE), 4);
     mbar_init(cx.bar(FIN_S), 1);
@@ -269,14 +279,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int row = warp * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const uint32_t peer_xrow = mapa_shared(sbase + OFF_X + row * XROW, peer);
-    const uint32_t peer_xfull = mapa_shared(cx.bar(XFULL), peer);
+    const uint32_t peer_xready = mapa_shared(cx.bar(XREADY), peer);
     const uint32_t peer_xfree = mapa_shared(cx.bar(XFREE), peer);
     const uint32_t my_xrow = sbase + OFF_X + row * XROW;
     const int xs = row & 15;  // 16-byte unit swizzle of the exchanged rows
     float* lse_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.lse_part);
     float* lbuf = reinterpret_cast<float*>(smem + OFF_L);
     const float c = p.scale_log2;
-    if (lane == 0) mbar_expect_tx(cx.bar(XFULL), 32 * XROW);  // armed for the first page
     // the RoPE query columns of sequence s, this thread's row, into registers
     uint4 qr[8];
     auto fetch_qr = [&](int s) {
@@ -326,23 +335,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(cx.bar(SFREE + sb));
-        // exchange: ours into the peer's buffer once it has consumed the last
-        // one, theirs from ours
+        // exchange: each CTA puts its partial in its own buffer (once the
+        // peer has read the previous one) and reads the peer's from the
+        // peer's buffer; per page only the 2 x 128 arrivals cross the pair,
+        // every data byte is a plain store and a distributed shared load
         ok = cx.warp_wait_cluster(XFREE, (it & 1) ^ 1, lane);
         if (!ok) break;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          st_async_v4(peer_xrow + ((u ^ xs) << 4), sa[4 * u], sa[4 * u + 1], sa[4 * u + 2],
-                      sa[4 * u + 3], peer_xfull);
+          sts_v4(my_xrow + ((u ^ xs) << 4), sa[4 * u], sa[4 * u + 1], sa[4 * u + 2], sa[4 * u + 3]);
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          st_async_v4(peer_xrow + (((8 + u) ^ xs) << 4), sc[4 * u], sc[4 * u + 1], sc[4 * u + 2],
-                      sc[4 * u + 3], peer_xfull);
-        ok = cx.warp_wait_cluster(XFULL, it & 1, lane);
+          sts_v4(my_xrow + (((8 + u) ^ xs) << 4), sc[4 * u], sc[4 * u + 1], sc[4 * u + 2],
+                 sc[4 * u + 3]);
+        mbar_arrive_remote(peer_xready);  // release: our row is visible to the peer
+        ok = cx.warp_wait_cluster(XREADY, it & 1, lane);
         if (!ok) break;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint4 x = lds_v4(my_xrow + ((u ^ xs) << 4));
+          const uint4 x = ld_cluster_v4(peer_xrow + ((u ^ xs) << 4));
           sa[4 * u] = __float_as_uint(__uint_as_float(sa[4 * u]) + __uint_as_float(x.x));
           sa[4 * u + 1] = __float_as_uint(__uint_as_float(sa[4 * u + 1]) + __uint_as_float(x.y));
           sa[4 * u + 2] = __float_as_uint(__uint_as_float(sa[4 * u + 2]) + __uint_as_float(x.z));
@@ -350,17 +361,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint4 x = lds_v4(my_xrow + (((8 + u) ^ xs) << 4));
+          const uint4 x = ld_cluster_v4(peer_xrow + (((8 + u) ^ xs) << 4));
           sc[4 * u] = __float_as_uint(__uint_as_float(sc[4 * u]) + __uint_as_float(x.x));
           sc[4 * u + 1] = __float_as_uint(__uint_as_float(sc[4 * u + 1]) + __uint_as_float(x.y));
           sc[4 * u + 2] = __float_as_uint(__uint_as_float(sc[4 * u + 2]) + __uint_as_float(x.z));
           sc[4 * u + 3] = __float_as_uint(__uint_as_float(sc[4 * u + 3]) + __uint_as_float(x.w));
         }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_remote(peer_xfree);                  // our rows of the buffer are free
-          mbar_expect_tx(cx.bar(XFULL), 32 * XROW);      // armed for the next page
-        }
+        mbar_arrive_remote(peer_xfree);  // we are done with the peer's buffer
 
         // online softmax (log2 units), both CTAs on the same S
         const int nvalid = min(PAGE, sg.len - (sg.p0 + j) * PAGE);
@@ -468,7 +475,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       for (int pb = sg.p0; ok && pb < sg.p1; pb += 32) {
         int blk = 0;
         if (pb + lane < sg.p1) {
-          blk = p.block_table[(size_t)s * p.max_pages + pb + lane];
+          blk = p.block_table[(size_t)(s / p.bt_div) * p.max_pages + pb + lane];
           if (blk < 0 || blk >= p.num_pages) {
             report(p.dev_status, MLA_DEV_BAD_BLOCK);
             blk = 0;
@@ -748,7 +755,7 @@ int tc_split_workers(int sms) {
 cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t* block_table,
                             int max_pages, int num_pages, int B, int workers, float scale,
                             const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
-                            int32_t* dev_status, cudaStream_t s) {
+                            int32_t* dev_status, int bt_div, cudaStream_t s) {
   CUtensorMap tm_cache, tm_q;
   cudaError_t e = tcs::make_map(&tm_cache, cache, (uint64_t)num_pages * tcs::PAGE, tcs::PAGE);
   if (e != cudaSuccess) return e;
@@ -765,6 +772,7 @@ cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t*
   p.max_pages = max_pages;
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.bt_div = bt_div > 0 ? bt_div : 1;
   p.withhold = tcs::g_withhold;
   static unsigned long long smem_done = 0;
   e = set_max_smem_once((const void*)tcs::tc_split_decode_kernel, (int)tcs::SMEM_BYTES, smem_done);

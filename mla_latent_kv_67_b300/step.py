@@ -5,10 +5,14 @@
 step on the current stream:
 
   attn    : absorb_q -> plan -> decode_attn -> combine -> absorb_out
+            (with q_len > 1: q_len new tokens per sequence, B * q_len query
+            rows, the _mtp plan and decode calls)
   layer   : append_latent -> project_q -> absorb_q -> plan -> decode_attn
             -> combine -> absorb_out -> out_proj
   prefill : append_latent (all ctx tokens) -> project_q (last token) ->
             absorb_q -> plan -> decode_attn -> combine -> absorb_out
+  layer, fused weights: append_latent -> project_q_absorbed (writes q_cat)
+            -> plan -> decode_attn -> combine -> out_proj_absorbed
 """
 from __future__ import annotations
 
@@ -66,16 +70,27 @@ class DecodeStep:
             self.c_q = (torch.empty((B, wl.d_cq), dtype=tdt, device=dev) if wl.d_cq else None)
             self.q = torch.empty((B, n_h, wl.d_h + wl.d_r), dtype=tdt, device=dev)
             self.w_o = W("w_o") if wl.mode == "layer" else None
+            if wl.fused:
+                # W^UK and W^UV folded into the neighbouring weights once
+                assert wl.mode == "layer"
+                K = wl.d_cq or wl.d_model
+                self.w_fused_q = torch.empty((n_h * (wl.d_c + wl.d_r), K), dtype=tdt, device=dev)
+                M.mla_fuse_query_weights(self.w_uq_qr, self.w_uk, self.w_fused_q, self.dims)
+                self.w_fused_o = torch.empty((wl.d_model, n_h * wl.d_c), dtype=tdt, device=dev)
+                M.mla_fuse_output_weights(self.w_o, self.w_uv, self.w_fused_o, self.dims)
+                self.o_lat_lowp = torch.empty((B, n_h * wl.d_c), dtype=tdt, device=dev)
         else:
             self.q = to_device(synth.storage(wl, synth.query(wl)), wl, dev)
-        self.q_cat = torch.empty((B, n_h, wl.d_c + wl.d_r), dtype=tdt, device=dev)
-        ws = M.mla_decode_workspace_size(B, self.dtype, self.dims)
+        assert wl.q_len == 1 or wl.mode == "attn", "several new tokens: attention-only workloads"
+        R = B * wl.q_len  # query rows
+        self.q_cat = torch.empty((R, n_h, wl.d_c + wl.d_r), dtype=tdt, device=dev)
+        ws = M.mla_decode_workspace_size(R, self.dtype, self.dims)
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
-        self.o_lat = torch.empty((B, n_h, wl.d_c), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((B, n_h), dtype=torch.float32, device=dev)
+        self.o_lat = torch.empty((R, n_h, wl.d_c), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((R, n_h), dtype=torch.float32, device=dev)
         if out_dtype is None:
             out_dtype = tdt if wl.mode == "layer" else torch.float32
-        self.o = torch.empty((B, n_h * wl.d_v), dtype=out_dtype, device=dev)
+        self.o = torch.empty((R, n_h * wl.d_v), dtype=out_dtype, device=dev)
         self.u = (torch.empty((B, wl.d_model), dtype=torch.float32, device=dev)
                   if wl.mode == "layer" else None)
         self.max_pages = bt.shape[1]
@@ -99,12 +114,22 @@ class DecodeStep:
         M.mla_absorb_q(self.q, self.w_uk, self.q_cat, self.dims)
 
     def plan(self):
-        M.mla_plan_decode(self.seq_lens, self.max_pages, self.workspace, self.dtype, self.dims,
-                          self.dev_status)
+        if self.wl.q_len > 1:
+            M.mla_plan_decode_mtp(self.seq_lens, self.wl.q_len, self.max_pages, self.workspace,
+                                  self.dtype, self.dims, self.dev_status)
+        else:
+            M.mla_plan_decode(self.seq_lens, self.max_pages, self.workspace, self.dtype,
+                              self.dims, self.dev_status)
 
     def attend(self):
-        M.mla_decode_attn(self.q_cat, self.cache, self.block_table, self.seq_lens, self.wl.scale,
-                          self.workspace, self.o_lat, self.lse, self.dims, self.dev_status)
+        if self.wl.q_len > 1:
+            M.mla_decode_attn_mtp(self.q_cat, self.cache, self.block_table, self.seq_lens,
+                                  self.wl.q_len, self.wl.scale, self.workspace, self.o_lat,
+                                  self.lse, self.dims, self.dev_status)
+        else:
+            M.mla_decode_attn(self.q_cat, self.cache, self.block_table, self.seq_lens,
+                              self.wl.scale, self.workspace, self.o_lat, self.lse, self.dims,
+                              self.dev_status)
 
     def combine(self):
         M.mla_combine(self.workspace, self.o_lat, self.lse, self.dtype, self.dims)
@@ -119,7 +144,17 @@ class DecodeStep:
     def out_proj(self):
         M.mla_out_proj(self.o, self.w_o, self.u, self.dims)
 
+    def project_absorbed(self):
+        M.mla_project_q_absorbed(self.x_q, self.w_dq, self.w_fused_q, self.q_pos, self.rope,
+                                 self.c_q, self.q_cat, self.dims, self.dev_status)
+
+    def out_absorbed(self):
+        M.mla_out_proj_absorbed(self.o_lat, self.o_lat_lowp, self.w_fused_o, self.u, self.dims)
+
     def stages(self):
+        if self.wl.fused:
+            return [self.append, self.project_absorbed, self.plan, self.attend, self.combine,
+                    self.out_absorbed]
         s = []
         if self.wl.mode in ("layer", "prefill"):
             s += [self.append, self.project]

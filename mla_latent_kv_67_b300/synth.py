@@ -72,6 +72,8 @@ class Workload:
     shuffle_pages: bool = True
     spare_pages: int = 0
     lens: tuple[int, ...] | None = None   # explicit per-sequence lengths
+    q_len: int = 1                        # new tokens decoded per sequence at once
+    fused: bool = False                   # full layer with W^UK / W^UV folded into W^UQ / W^O
 
     @property
     def row_width(self) -> int:
@@ -101,6 +103,17 @@ WORKLOADS: dict[str, Workload] = {
     "dsv2_layer_b64_ctx32k": Workload(
         name="dsv2_layer_b64_ctx32k", batch=64, d_model=5120, d_cq=1536,
         ctx=32768, mode="layer", seed=67005),
+}
+
+# Beyond the five: two new tokens per sequence decoded at once (multi-token
+# prediction / a speculative draft), on the batch-32, 4096-token shape.
+# The full-layer step again with the absorption folded into the weights
+# once (W~^Q, W~^O) instead of applied per head at every step.
+EXTRA_WORKLOADS: dict[str, Workload] = {
+    "dsv2_b32_ctx4k_mtp2": Workload(name="dsv2_b32_ctx4k_mtp2", batch=32, ctx=4096, q_len=2,
+                                    seed=67006),
+    "dsv2_layer_b64_ctx32k_fused": WORKLOADS["dsv2_layer_b64_ctx32k"].replace(
+        name="dsv2_layer_b64_ctx32k_fused", fused=True),
 }
 
 
@@ -220,9 +233,10 @@ def paged_cache(wl: Workload, lens: np.ndarray, bt: np.ndarray, pool: int) -> np
 
 # ------------------------------------------------------- queries / weights
 def query(wl: Workload) -> np.ndarray:
-    """Drawn queries ``[B][n_h][d_h+d_r]`` (no-PE part first, RoPE part
-    last), treated as already rotated."""
-    return _draw(wl, _rng(wl, _S_QUERY), (wl.batch, wl.n_h, wl.d_h + wl.d_r))
+    """Drawn queries ``[B * q_len][n_h][d_h+d_r]`` (no-PE part first, RoPE
+    part last; row ``b * q_len + t`` is new token t of sequence b), treated
+    as already rotated."""
+    return _draw(wl, _rng(wl, _S_QUERY), (wl.batch * wl.q_len, wl.n_h, wl.d_h + wl.d_r))
 
 
 def tokens(wl: Workload) -> np.ndarray:

@@ -98,7 +98,8 @@ class Expected:
         return pos, c, k
 
     def query(self, b: int):
-        """(q_c [n_h, d_h], q_r [n_h, d_r]) of sequence b's decode token."""
+        """(q_c [n_h, d_h], q_r [n_h, d_r]) of query row b (sequence b, or
+        with several new tokens per sequence row b = sequence * q_len + t)."""
         wl = self.wl
         if wl.mode == "attn":
             return self.q[b, :, :wl.d_h], self.q[b, :, wl.d_h:]
@@ -120,14 +121,20 @@ class Expected:
         return c, k
 
     def seq(self, b: int, explicit_heads=None, drop_rows=None):
-        """Oracle outputs of sequence b: absorbed (all heads) and, for
-        ``explicit_heads``, the explicit non-absorbed definition.
-        ``drop_rows`` (a slice of token indices) removes those cached tokens
-        from the oracle's input: a planted mistake for checking that the
-        parity gate rejects a wrong answer."""
+        """Oracle outputs of query row b (sequence b; with q_len new tokens
+        per sequence, row b = sequence * q_len + t, which sees the first
+        ``multi_token_lengths(len, q_len)[t]`` cached rows): absorbed (all
+        heads) and, for ``explicit_heads``, the explicit non-absorbed
+        definition. ``drop_rows`` (a slice of token indices) removes those
+        cached tokens from the oracle's input: a planted mistake for checking
+        that the parity gate rejects a wrong answer."""
         wl = self.wl
         q_c, q_r = self.query(b)
-        c, k = self.cache_rows(b)
+        seq, t = divmod(b, wl.q_len)
+        c, k = self.cache_rows(seq)
+        if wl.q_len > 1:
+            n = int(O.multi_token_lengths(len(c), wl.q_len)[t])
+            c, k = c[:n], k[:n]
         if drop_rows is not None:
             keep = np.ones(len(c), bool)
             keep[drop_rows] = False
