@@ -77,6 +77,17 @@ def peaks():
     return 6400.0, 1800.0, "fallback"
 
 
+def algorithmic_prefill(wl):
+    """Algorithmic bytes and FLOPs of one prefill attention launch over a
+    prompt of N tokens: q, k_nope, v and the latent rows read once, o
+    written once; FLOPs of the causal products (token i: i + 1 keys, scores
+    over d_h + d_r, output over d_v)."""
+    N = wl.ctx
+    b = N * wl.n_h * ((wl.d_h + wl.d_r) + wl.d_h + wl.d_v + wl.d_v) * 2 + N * (wl.d_c + wl.d_r) * 2
+    pairs = N * (N + 1) // 2
+    return b, pairs * wl.n_h * 2 * (wl.d_h + wl.d_r + wl.d_v)
+
+
 def algorithmic(wl, lens):
     """Algorithmic bytes and FLOPs of one decode_attn launch: each cached row
     (c_kv | k_R) read once, q_cat read once, o_lat written once; FLOPs of the
@@ -370,24 +381,30 @@ def measure_workload(wl, dev, K, W, flush, stream, hbm, tflops, barrier=None, sa
         stages[f.__name__] = time_graph(gs, K, flush, stream) * 1e3
     torch.cuda.synchronize()
     assert st.status() == 0, f"{wl.name}: device status {st.status():#x}"
-    kernel_us = stages["attend"]
-    alg_bytes, alg_flops = algorithmic(wl, st.lens_np)
+    prefill = wl.mode == "prefill_mha"
+    kernel_us = stages["prefill" if prefill else "attend"]
+    alg_bytes, alg_flops = algorithmic_prefill(wl) if prefill else algorithmic(wl, st.lens_np)
     t_hbm = alg_bytes / (hbm * 1e9)
     t_flop = alg_flops / (tflops * 1e12)
     achieved = alg_bytes / (kernel_us * 1e-6) / 1e9
     tensor = alg_flops / (kernel_us * 1e-6) / 1e12
     path = M.mla_decode_path(st.dtype, st.dims)
-    roof = {"bound": "hbm" if t_hbm >= t_flop else "tensor", "achieved": achieved, "peak": hbm,
-            "unit": "GB/s", "frac": achieved / hbm,
+    tensor_bound = t_flop > t_hbm
+    roof = {"bound": "tensor" if tensor_bound else "hbm",
+            "achieved": tensor if tensor_bound else achieved,
+            "peak": tflops if tensor_bound else hbm,
+            "unit": "TFLOP/s" if tensor_bound else "GB/s",
+            "frac": tensor / tflops if tensor_bound else achieved / hbm,
             "traffic": DECODE_TRAFFIC.get(wl.name) if path == 1 else None,
-            "kernel": "mla_decode_attn", "kernel_us": kernel_us,
+            "kernel": "mla_prefill_attn" if prefill else "mla_decode_attn", "kernel_us": kernel_us,
             "alg_bytes": alg_bytes, "alg_flops": alg_flops,
             "tensor_tflops": tensor, "tensor_peak": tflops, "tensor_frac": tensor / tflops,
             "roofline_us": max(t_hbm, t_flop) * 1e6,
             "frac_of_roofline": max(t_hbm, t_flop) * 1e6 / kernel_us}
     return st, g, {"step_us": step_ms * 1e3, "stages_us": stages, "roofline": roof,
                    "decode_kernel": DECODE_KERNELS.get(path, "simt"),
-                   "step_roofline": step_roofline(wl, st.lens_np, hbm, tflops, step_ms * 1e3)}
+                   "step_roofline": None if prefill else
+                   step_roofline(wl, st.lens_np, hbm, tflops, step_ms * 1e3)}
 
 
 def main():
@@ -515,7 +532,7 @@ def main():
     roof["timing"] = "decode launch alone in its own CUDA graph, L2 flushed before each"
     launches = sum({"absorb_q": 1 if res["decode_kernel"] != "simt" else 2,
                     "project": 2 if wl.d_cq else 1, "project_absorbed": 2 if wl.d_cq else 1,
-                    "out_absorbed": 2}.get(f.__name__, 1) for f in stages)
+                    "out_absorbed": 2, "expand": 2}.get(f.__name__, 1) for f in stages)
     line = {
         "metric": METRIC, "value": step_ms * 1e3, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False,
@@ -567,7 +584,7 @@ def main():
 # measured beside the headline workload in the same run (the tiny fp32
 # workload is a parity case only)
 OTHER_WORKLOADS = ("dsv2_b4_ctx128k", "dsv2_b128_ragged", "dsv2_layer_b64_ctx32k",
-                   "dsv2_layer_b64_ctx32k_fused", "dsv2_b32_ctx4k_mtp2")
+                   "dsv2_layer_b64_ctx32k_fused", "dsv2_b32_ctx4k_mtp2", "dsv2_prefill_4k")
 
 
 if __name__ == "__main__":

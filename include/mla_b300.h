@@ -230,6 +230,36 @@ mla_status mla_combine_absorb_out(const void* workspace, size_t ws_bytes, int B,
 mla_status mla_out_proj(const void* o, const void* w_o, float* u, int B, mla_dtype dtype,
                         const mla_dims* dims, void* stream);
 
+/* Prefill in the MHA form -- "kv-cache 的优化学习" (cnblogs), closing
+ * note: the cache holds the MLA form; a prompt is expanded to per-head keys
+ * and values (MHA) for prefill and decoding stays in the latent form; the
+ * DeepSeek-V2 MLA page 2.1 gives the expansion k^C = W^UK c, v^C = W^UV c and
+ * 3.2 the key [k^C_h ; k^R] with the RoPE key shared by all heads. For one
+ * sequence of N prompt tokens already appended to the cache:
+ *   mla_gather_latent   rows [N][d_c + d_r] = the cache rows of positions
+ *                       0..N-1 of sequence `seq` (dense copy).
+ *   mla_expand_kv       k_nope [N][n_h][d_h] = c W^UK_h^T and
+ *                       v [N][n_h][d_v] = c W^UV_h^T for every head (c =
+ *                       rows[:, :d_c]); fp32 accumulation, stored in `dtype`.
+ *   mla_prefill_attn    o [N][n_h][d_v] (bf16) and lse [N][n_h] (float, may
+ *                       be NULL): token i attends to tokens j <= i,
+ *                       s_j = (q_i,h . [k_nope_j,h ; k_R,j]) * softmax_scale,
+ *                       with q [N][n_h][d_h + d_r] from mla_project_q (T = N).
+ *                       bf16 tensor-core products, fp32 accumulation and
+ *                       softmax, probabilities rounded to bf16 for P.V.
+ *                       Built for bf16 with n_h = 128, d_h = d_v = 128,
+ *                       d_r = 64, d_c = 512 (else MLA_ERR_UNSUPPORTED). */
+mla_status mla_gather_latent(const void* cache, const int32_t* block_table, int max_pages,
+                             int num_pages, int seq, int n_tokens, void* rows, mla_dtype dtype,
+                             const mla_dims* dims, int32_t* dev_status, void* stream);
+mla_status mla_expand_kv(const void* rows, const void* w_uk, const void* w_uv, void* k_nope,
+                         void* v, int n_tokens, mla_dtype dtype, const mla_dims* dims,
+                         void* stream);
+mla_status mla_prefill_attn(const void* q, const void* k_nope, const void* rows, const void* v,
+                            void* o, float* lse, int n_tokens, float softmax_scale,
+                            mla_dtype dtype, const mla_dims* dims, int32_t* dev_status,
+                            void* stream);
+
 /* Fused absorption -- DeepSeek-V2 MLA page 2.2, the form that folds the
  * up-projections into the neighbouring weights once, ahead of decoding:
  * W~^Q = W^UQ^T W^UK (query side) and W~^O = W^O W^UV (output side). The

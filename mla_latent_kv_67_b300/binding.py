@@ -65,6 +65,9 @@ _SIGS = {
     "mla_tc_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
     "mla_out_proj": (_I, [_P, _P, _P, _I, _I, _DIMS, _P]),
     "mla_fuse_query_weights": (_I, [_P, _P, _P, _I, _DIMS, _P]),
+    "mla_gather_latent": (_I, [_P, _P, _I, _I, _I, _I, _P, _I, _DIMS, _P, _P]),
+    "mla_expand_kv": (_I, [_P, _P, _P, _P, _P, _I, _I, _DIMS, _P]),
+    "mla_prefill_attn": (_I, [_P, _P, _P, _P, _P, _P, _I, _F, _I, _DIMS, _P, _P]),
     "mla_project_q_absorbed": (_I, [_P, _P, _P, _P, _I, _P, _I, _P, _P, _I, _DIMS, _P, _P]),
     "mla_fuse_output_weights": (_I, [_P, _P, _P, _I, _DIMS, _P]),
     "mla_out_proj_absorbed": (_I, [_P, _P, _P, _P, _I, _I, _DIMS, _P]),
@@ -349,3 +352,41 @@ def mla_out_proj_absorbed(o_lat, o_lat_lowp, w_fused_o, u, dims: Dims, stream=No
         _ptr(w_fused_o, shape=(dims.d_model, dims.n_h * dims.d_c), name="w_fused_o"),
         _ptr(u, torch.float32, (B, dims.d_model), "u"), B, dt, ctypes.byref(dims),
         _stream(stream)))
+
+
+# ----------------------------------------------------------------- prefill
+def mla_gather_latent(cache, block_table, seq: int, rows, dims: Dims, dev_status=None,
+                      stream=None) -> None:
+    N = rows.shape[0]
+    B, max_pages = block_table.shape
+    _check(lib().mla_gather_latent(
+        _ptr(cache, shape=(cache.shape[0], dims.page_size, dims.d_c + dims.d_r), name="cache"),
+        _ptr(block_table, torch.int32, name="block_table"), max_pages, cache.shape[0], seq, N,
+        _ptr(rows, cache.dtype, (N, dims.d_c + dims.d_r), "rows"), _dt(cache), ctypes.byref(dims),
+        _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
+
+
+def mla_expand_kv(rows, w_uk, w_uv, k_nope, v, dims: Dims, stream=None) -> None:
+    N = rows.shape[0]
+    dt = _dt(rows)
+    _check(lib().mla_expand_kv(
+        _ptr(rows, shape=(N, dims.d_c + dims.d_r), name="rows"),
+        _ptr(w_uk, rows.dtype, (dims.n_h * dims.d_h, dims.d_c), "w_uk"),
+        _ptr(w_uv, rows.dtype, (dims.n_h * dims.d_v, dims.d_c), "w_uv"),
+        _ptr(k_nope, rows.dtype, (N, dims.n_h, dims.d_h), "k_nope"),
+        _ptr(v, rows.dtype, (N, dims.n_h, dims.d_v), "v"), N, dt, ctypes.byref(dims),
+        _stream(stream)))
+
+
+def mla_prefill_attn(q, k_nope, rows, v, o, lse, scale: float, dims: Dims, dev_status=None,
+                     stream=None) -> None:
+    N = q.shape[0]
+    dt = _dt(q)
+    _check(lib().mla_prefill_attn(
+        _ptr(q, shape=(N, dims.n_h, dims.d_h + dims.d_r), name="q"),
+        _ptr(k_nope, q.dtype, (N, dims.n_h, dims.d_h), "k_nope"),
+        _ptr(rows, q.dtype, (N, dims.d_c + dims.d_r), "rows"),
+        _ptr(v, q.dtype, (N, dims.n_h, dims.d_v), "v"),
+        _ptr(o, torch.bfloat16, (N, dims.n_h, dims.d_v), "o"),
+        _ptr(lse, torch.float32, (N, dims.n_h), "lse"), N, scale, dt, ctypes.byref(dims),
+        _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))

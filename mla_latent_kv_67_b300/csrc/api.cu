@@ -347,6 +347,71 @@ mla_status mla_out_proj_absorbed(const float* o_lat, void* o_lat_lowp, const voi
   return cuda_status(projection(g, S(stream)), "out_proj_absorbed");
 }
 
+mla_status mla_gather_latent(const void* cache, const int32_t* block_table, int max_pages,
+                             int num_pages, int seq, int n_tokens, void* rows, mla_dtype dtype,
+                             const mla_dims* dims, int32_t* dev_status, void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(n_tokens >= 0 && seq >= 0, "seq and n_tokens must be >= 0");
+  if (n_tokens == 0) return MLA_OK;
+  REQUIRE(cache && block_table && rows, "NULL tensor argument");
+  REQUIRE(max_pages > 0 && num_pages > 0, "max_pages and num_pages must be > 0");
+  REQUIRE(n_tokens <= max_pages * dims->page_size, "n_tokens past the block table");
+  const int esz = dtype == MLA_F32 ? 4 : 2;
+  REQUIRE(((dims->d_c + dims->d_r) * esz) % 16 == 0, "row width must be a multiple of 16 bytes");
+  return cuda_status(launch_gather_rows(cache, block_table, max_pages, num_pages, dims->page_size,
+                                        seq, n_tokens, dims->d_c + dims->d_r, esz, rows,
+                                        dev_status, S(stream)),
+                     "gather_latent");
+}
+
+mla_status mla_expand_kv(const void* rows, const void* w_uk, const void* w_uv, void* k_nope,
+                         void* v, int n_tokens, mla_dtype dtype, const mla_dims* dims,
+                         void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(n_tokens >= 0, "n_tokens must be >= 0");
+  if (n_tokens == 0) return MLA_OK;
+  REQUIRE(rows && w_uk && w_uv && k_nope && v, "NULL tensor argument");
+  const int f32 = dtype == MLA_F32;
+  const int W = dims->d_c + dims->d_r;
+  // k_nope[t][h*d_h + i] = sum_c rows[t][c] W^UK[h*d_h + i][c], and the same for W^UV
+  for (int which = 0; which < 2; ++which) {
+    GemmArgs g = {};
+    g.a = rows; g.a_ms = W; g.a_f32 = f32;
+    g.w = which == 0 ? w_uk : w_uv; g.w_ns = dims->d_c; g.w_ks = 1; g.w_f32 = f32;
+    g.G = 1; g.M = n_tokens; g.N = dims->n_h * (which == 0 ? dims->d_h : dims->d_v);
+    g.K = dims->d_c;
+    g.epi = EPI_STORE; g.out = which == 0 ? k_nope : v; g.o_ms = g.N; g.o_f32 = f32;
+    if ((st = cuda_status(projection(g, S(stream)), which == 0 ? "expand_kv/K" : "expand_kv/V")) !=
+        MLA_OK)
+      return st;
+  }
+  return MLA_OK;
+}
+
+mla_status mla_prefill_attn(const void* q, const void* k_nope, const void* rows, const void* v,
+                            void* o, float* lse, int n_tokens, float softmax_scale,
+                            mla_dtype dtype, const mla_dims* dims, int32_t* dev_status,
+                            void* stream) {
+  mla_status st = check_dims(dims);
+  if (st != MLA_OK) return st;
+  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  REQUIRE(n_tokens >= 0, "n_tokens must be >= 0");
+  if (n_tokens == 0) return MLA_OK;
+  REQUIRE(q && k_nope && rows && v && o, "NULL tensor argument");
+  if (dtype != MLA_BF16 ||
+      !tc_prefill_supported(dims->n_h, dims->d_h, dims->d_r, dims->d_c, dims->d_v))
+    return fail(MLA_ERR_UNSUPPORTED,
+                "prefill attention is built for bf16 and n_h=128, d_h=d_v=128, d_r=64, d_c=512 "
+                "on an sm_103 device");
+  return cuda_status(tc_prefill_launch(q, k_nope, rows, v, o, lse, n_tokens, softmax_scale,
+                                       dev_status, S(stream)),
+                     "prefill_attn (tcgen05)");
+}
+
 mla_status mla_absorb_q(const void* q, const void* w_uk, void* q_cat, int B, mla_dtype dtype,
                         const mla_dims* dims, void* stream) {
   mla_status st = check_dims(dims);

@@ -46,6 +46,11 @@ cudaError_t launch_rope_table(float* cs, int max_pos, int d_r, double base, cuda
 cudaError_t launch_copy_rows(const void* src, long long src_gs, long long src_rs, void* dst,
                              long long dst_gs, long long dst_rs, int G, int rows, int cols,
                              int esz, cudaStream_t s);
+// rows[t] = the cache row of position t of sequence `seq`, t < n (block ids
+// outside the pool are reported and give a zero row).
+cudaError_t launch_gather_rows(const void* cache, const int32_t* block_table, int max_pages,
+                               int num_pages, int page_size, int seq, int n, int width, int esz,
+                               void* rows, int32_t* dev_status, cudaStream_t s);
 // dst[i] = bf16(src[i]) for i < n.
 cudaError_t launch_to_bf16(const float* src, void* dst, long long n, cudaStream_t s);
 

@@ -160,6 +160,34 @@ cudaError_t launch_copy_rows(const void* src, long long src_gs, long long src_rs
   return cudaGetLastError();
 }
 
+__global__ void gather_rows_kernel(const uint4* __restrict__ cache, const int32_t* __restrict__ bt,
+                                   int max_pages, int num_pages, int page_size, int seq, int n,
+                                   int w16, uint4* __restrict__ rows, int32_t* dev_status) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)n * w16;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / w16), u = (int)(i % w16);
+    const int blk = bt[(size_t)seq * max_pages + t / page_size];
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (blk < 0 || blk >= num_pages) report(dev_status, MLA_DEV_BAD_BLOCK);
+    else v = cache[((size_t)blk * page_size + t % page_size) * w16 + u];
+    rows[i] = v;
+  }
+}
+
+cudaError_t launch_gather_rows(const void* cache, const int32_t* block_table, int max_pages,
+                               int num_pages, int page_size, int seq, int n, int width, int esz,
+                               void* rows, int32_t* dev_status, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  if ((width * esz) % 16 != 0) return cudaErrorInvalidValue;
+  const int w16 = width * esz / 16;
+  const long long total = (long long)n * w16;
+  const int blocks = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
+  gather_rows_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(cache), block_table,
+                                            max_pages, num_pages, page_size, seq, n, w16,
+                                            reinterpret_cast<uint4*>(rows), dev_status);
+  return cudaGetLastError();
+}
+
 __global__ void to_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, long long n4) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {

@@ -35,6 +35,14 @@ cudaError_t tc_absorb_out_merge_launch(const void* ws, const WorkspaceLayout& L,
                                        float* lse, const void* w_uv, void* o, int out_f32, int B,
                                        int32_t* dev_status, cudaStream_t s);
 
+// Causal prefill attention in the MHA form (tc_prefill.cu): DeepSeek-V2
+// shapes, bf16. q [N][128][192], k_nope [N][128][128], rows [N][576] (k_R =
+// columns 512..575), v [N][128][128] -> o [N][128][128] bf16, lse [N][128].
+bool tc_prefill_supported(int n_h, int d_h, int d_r, int d_c, int d_v);
+cudaError_t tc_prefill_launch(const void* q, const void* k_nope, const void* rows, const void* v,
+                              void* o, float* lse, int N, float scale, int32_t* dev_status,
+                              cudaStream_t s);
+
 // One page of the decode's tensor-core data path without softmax:
 // s_out[128][64] = q_cat[128][576] . page[64][576]^T and
 // o_out[128][256] = pmat[128][64] . page[:, 256 r : 256 r + 256].

@@ -15,8 +15,8 @@
 // (40 KB / 32 KB instead of the whole 72 KB row block), computes the partial
 // score S_r over its columns, and the two partials are exchanged through
 // distributed shared memory (each CTA stores its partial in its own shared
-// memory and loads the peer's; two barriers per page with one remote
-// arrival per row synchronise the pair): both CTAs then hold
+// memory and loads the peer's; per page one remote arrival says "ours is
+// ready" and one says "we have read yours"): both CTAs then hold
 // S = S_0 + S_1, bit for bit the same, and run the same online softmax, so
 // each can multiply the probabilities into its own half of O. At a sequence's end each CTA writes
 // its own 128 KB of O, so the write-out of a split partial takes half as
@@ -76,9 +76,11 @@ enum {
   QFULL = PFREE + 2,     // Q latent half of the sequence landed
   QFREE = QFULL + 1,     // last S of the sequence done (commit)
   QRREADY = QFREE + 1,   // RoPE query in TMEM (4 warps; rank 0)
-  XREADY = QRREADY + 1,  // the peer's partial S is in its buffer (128 remote arrivals)
-  XFREE = XREADY + 1,    // the peer has read our partial S (128 remote arrivals)
-  LREADY = XFREE + 1,    // [2] 1 / l of a sequence written (4 softmax warps)
+  XREADY = QRREADY + 1,  // the peer's partial S is in its buffer (1 remote arrival)
+  XFREE = XREADY + 1,    // the peer has read our partial S (1 remote arrival)
+  XSTORED = XFREE + 1,   // our 4 softmax warps stored their rows of the partial S
+  XREAD = XSTORED + 1,   // our 4 softmax warps read their rows of the peer's
+  LREADY = XREAD + 1,    // [2] 1 / l of a sequence written (4 softmax warps)
   LFREE = LREADY + 2,    // [2] 1 / l read by the 4 epilogue warps
   ODONE = LFREE + 2,     // last PV of a sequence done (commit)
   OFREE = ODONE + 1,     // O written out (4 epilogue warps)
@@ -254,8 +256,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mbar_init(cx.bar(QFULL), 1);
     mbar_init(cx.bar(QFREE), 1);
     mbar_init(cx.bar(QRREADY), 4);
-    mbar_init(cx.bar(XREADY), NH);
-    mbar_init(cx.bar(XFREE), NH);
+    mbar_init(cx.bar(XREADY), 1);
+    mbar_init(cx.bar(XFREE), 1);
+    mbar_init(cx.bar(XSTORED), 4);
+    mbar_init(cx.bar(XREAD), 4);
     mbar_init(cx.bar(ODONE), 1);
     mbar_init(cx.bar(OFREE), 4);
     mbar_init(cx.bar(FIN_S), 1);
@@ -348,7 +352,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int u = 0; u < 8; ++u)
           sts_v4(my_xrow + (((8 + u) ^ xs) << 4), sc[4 * u], sc[4 * u + 1], sc[4 * u + 2],
                  sc[4 * u + 3]);
-        mbar_arrive_remote(peer_xready);  // release: our row is visible to the peer
+        // once all 128 rows are stored (each warp arrives on XSTORED), one
+        // release arrival on the peer's barrier makes them visible to it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cx.bar(XSTORED));
+        if (row == 0) {
+          ok = cx.wait(XSTORED, it & 1);
+          if (ok) mbar_arrive_remote(peer_xready);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
         ok = cx.warp_wait_cluster(XREADY, it & 1, lane);
         if (!ok) break;
 #pragma unroll
@@ -367,7 +380,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           sc[4 * u + 2] = __float_as_uint(__uint_as_float(sc[4 * u + 2]) + __uint_as_float(x.z));
           sc[4 * u + 3] = __float_as_uint(__uint_as_float(sc[4 * u + 3]) + __uint_as_float(x.w));
         }
-        mbar_arrive_remote(peer_xfree);  // we are done with the peer's buffer
+        // every row of the peer's buffer read (XREAD), then one arrival on
+        // the peer's XFREE
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cx.bar(XREAD));
+        if (row == 0) {
+          ok = cx.wait(XREAD, it & 1);
+          if (ok) mbar_arrive_remote(peer_xfree);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
 
         // online softmax (log2 units), both CTAs on the same S
         const int nvalid = min(PAGE, sg.len - (sg.p0 + j) * PAGE);

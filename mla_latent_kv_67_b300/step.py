@@ -13,6 +13,8 @@ step on the current stream:
             absorb_q -> plan -> decode_attn -> combine -> absorb_out
   layer, fused weights: append_latent -> project_q_absorbed (writes q_cat)
             -> plan -> decode_attn -> combine -> out_proj_absorbed
+  prefill_mha : append_latent (all ctx tokens) -> project_q (all tokens) ->
+            gather_latent -> expand_kv -> prefill_attn
 """
 from __future__ import annotations
 
@@ -47,7 +49,7 @@ class DecodeStep:
         B, n_h = wl.batch, wl.n_h
         W = lambda name: to_device(synth.storage(wl, synth.weight(wl, name)), wl, dev)
         self.w_uk, self.w_uv = W("w_uk"), W("w_uv")
-        if wl.mode in ("layer", "prefill"):
+        if wl.mode in ("layer", "prefill", "prefill_mha"):
             self.w_dkv_kr = to_device(synth.storage(wl, synth.joint_w_dkv_kr(
                 synth.weight(wl, "w_dkv"), synth.weight(wl, "w_kr"))), wl, dev)
             self.w_uq_qr = to_device(synth.storage(wl, synth.joint_w_uq_qr(
@@ -62,13 +64,19 @@ class DecodeStep:
                 self.append_seq = None
                 self.q_pos = self.append_pos
                 self.x_q = self.x
-            else:
+            elif wl.mode == "prefill":
                 self.append_pos = torch.arange(wl.ctx, dtype=torch.int32, device=dev)
                 self.append_seq = torch.zeros(wl.ctx, dtype=torch.int32, device=dev)
                 self.q_pos = self.append_pos[-1:].contiguous()
                 self.x_q = self.x[-1:].contiguous()
-            self.c_q = (torch.empty((B, wl.d_cq), dtype=tdt, device=dev) if wl.d_cq else None)
-            self.q = torch.empty((B, n_h, wl.d_h + wl.d_r), dtype=tdt, device=dev)
+            else:  # prefill_mha: every prompt token is a query
+                self.append_pos = torch.arange(wl.ctx, dtype=torch.int32, device=dev)
+                self.append_seq = torch.zeros(wl.ctx, dtype=torch.int32, device=dev)
+                self.q_pos = self.append_pos
+                self.x_q = self.x
+            T = wl.ctx if wl.mode == "prefill_mha" else B
+            self.c_q = (torch.empty((T, wl.d_cq), dtype=tdt, device=dev) if wl.d_cq else None)
+            self.q = torch.empty((T, n_h, wl.d_h + wl.d_r), dtype=tdt, device=dev)
             self.w_o = W("w_o") if wl.mode == "layer" else None
             if wl.fused:
                 # W^UK and W^UV folded into the neighbouring weights once
@@ -82,6 +90,13 @@ class DecodeStep:
         else:
             self.q = to_device(synth.storage(wl, synth.query(wl)), wl, dev)
         assert wl.q_len == 1 or wl.mode == "attn", "several new tokens: attention-only workloads"
+        if wl.mode == "prefill_mha":
+            N = wl.ctx
+            self.rows = torch.empty((N, wl.d_c + wl.d_r), dtype=tdt, device=dev)
+            self.k_nope = torch.empty((N, n_h, wl.d_h), dtype=tdt, device=dev)
+            self.v = torch.empty((N, n_h, wl.d_v), dtype=tdt, device=dev)
+            self.o_pf = torch.empty((N, n_h, wl.d_v), dtype=torch.bfloat16, device=dev)
+            self.lse_pf = torch.empty((N, n_h), dtype=torch.float32, device=dev)
         R = B * wl.q_len  # query rows
         self.q_cat = torch.empty((R, n_h, wl.d_c + wl.d_r), dtype=tdt, device=dev)
         ws = M.mla_decode_workspace_size(R, self.dtype, self.dims)
@@ -144,6 +159,16 @@ class DecodeStep:
     def out_proj(self):
         M.mla_out_proj(self.o, self.w_o, self.u, self.dims)
 
+    def gather(self):
+        M.mla_gather_latent(self.cache, self.block_table, 0, self.rows, self.dims, self.dev_status)
+
+    def expand(self):
+        M.mla_expand_kv(self.rows, self.w_uk, self.w_uv, self.k_nope, self.v, self.dims)
+
+    def prefill(self):
+        M.mla_prefill_attn(self.q, self.k_nope, self.rows, self.v, self.o_pf, self.lse_pf,
+                           self.wl.scale, self.dims, self.dev_status)
+
     def project_absorbed(self):
         M.mla_project_q_absorbed(self.x_q, self.w_dq, self.w_fused_q, self.q_pos, self.rope,
                                  self.c_q, self.q_cat, self.dims, self.dev_status)
@@ -152,6 +177,8 @@ class DecodeStep:
         M.mla_out_proj_absorbed(self.o_lat, self.o_lat_lowp, self.w_fused_o, self.u, self.dims)
 
     def stages(self):
+        if self.wl.mode == "prefill_mha":
+            return [self.append, self.project, self.gather, self.expand, self.prefill]
         if self.wl.fused:
             return [self.append, self.project_absorbed, self.plan, self.attend, self.combine,
                     self.out_absorbed]
@@ -171,6 +198,10 @@ class DecodeStep:
         """One step. The split plan depends only on the lengths, so it runs on
         a side stream next to the stages before attention (both streams
         join before the decode kernel; this also captures into a graph)."""
+        if self.wl.mode == "prefill_mha":
+            for f in self.stages():
+                f()
+            return
         main = torch.cuda.current_stream(self.q_cat.device)
         if self._side is None:
             self._side = torch.cuda.Stream(device=self.q_cat.device)
@@ -184,6 +215,8 @@ class DecodeStep:
                 f()
 
     def result(self) -> torch.Tensor:
+        if self.wl.mode == "prefill_mha":
+            return self.o_pf
         return self.u if self.wl.mode == "layer" else self.o
 
     def status(self) -> int:

@@ -51,6 +51,9 @@ class Workload:
       * ``"prefill"``- a single sequence whose whole cache is produced by the
                        append step from drawn x at positions 0..ctx-1; the
                        query is projected from the last token (no W^O).
+      * ``"prefill_mha"`` - the same single sequence, but every one of its
+                       ctx tokens is a query: causal attention in the MHA form
+                       over keys and values expanded from the latent rows.
     """
 
     name: str
@@ -114,6 +117,9 @@ EXTRA_WORKLOADS: dict[str, Workload] = {
                                     seed=67006),
     "dsv2_layer_b64_ctx32k_fused": WORKLOADS["dsv2_layer_b64_ctx32k"].replace(
         name="dsv2_layer_b64_ctx32k_fused", fused=True),
+    # a 4096-token prompt prefilled in the MHA form (DeepSeek-V2 shapes)
+    "dsv2_prefill_4k": Workload(name="dsv2_prefill_4k", batch=1, ctx=4096, d_model=5120,
+                                d_cq=1536, mode="prefill_mha", seed=67007, shuffle_pages=True),
 }
 
 
@@ -206,7 +212,7 @@ def drawn_rows(wl: Workload, lens: np.ndarray) -> np.ndarray:
         return lens.copy()
     if wl.mode == "layer":
         return lens - 1
-    return np.zeros_like(lens)
+    return np.zeros_like(lens)  # prefill modes: every row comes from the append step
 
 
 def paged_cache(wl: Workload, lens: np.ndarray, bt: np.ndarray, pool: int) -> np.ndarray:
@@ -240,8 +246,8 @@ def query(wl: Workload) -> np.ndarray:
 
 
 def tokens(wl: Workload) -> np.ndarray:
-    """Hidden states x: ``[ctx][d_model]`` (prefill) or ``[B][d_model]``."""
-    n = wl.ctx if wl.mode == "prefill" else wl.batch
+    """Hidden states x: ``[ctx][d_model]`` (prefill modes) or ``[B][d_model]``."""
+    n = wl.ctx if wl.mode in ("prefill", "prefill_mha") else wl.batch
     return _draw(wl, _rng(wl, _S_X), (n, wl.d_model))
 
 
