@@ -90,8 +90,8 @@ int pick_path(mla_dtype dt, const mla_dims* d) {
 int workers_for(int path) {
   const int sms = device_sms();
   if (sms <= 0) return 0;
-  if (path == 1) return tc_split_workers(sms);
-  if (path == 2) return tc_pair_workers(sms);
+  if (path == 1) return tc_pair_workers(sms);
+  if (path == 2) return tc_split_workers(sms);
   return sms;
 }
 
@@ -102,11 +102,11 @@ cudaError_t launch_decode(const DecodeSetup& ds, const void* q_cat, const void* 
                           const mla_dims* d, int32_t* dev_status, cudaStream_t s) {
   const int rows = B * ds.q_len;  // query rows
   if (ds.path == 1)
-    return tc_split_launch(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
-                           softmax_scale, ws, ds.L, o_lat, lse, dev_status, ds.q_len, s);
-  if (ds.path == 2)
     return tc_pair_launch(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
                           softmax_scale, ws, ds.L, o_lat, lse, dev_status, ds.q_len, s);
+  if (ds.path == 2)
+    return tc_split_launch(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
+                           softmax_scale, ws, ds.L, o_lat, lse, dev_status, ds.q_len, s);
   return launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
                             softmax_scale, ws, ds.L, o_lat, lse, d->n_h, d->d_c, d->d_r,
                             d->page_size, dtype == MLA_F32, dev_status, ds.q_len, s);

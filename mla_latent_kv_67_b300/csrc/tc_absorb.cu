@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(128)
     }
   }
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  const bool done = wait_bar(bar_mma, 0, dev_status);
+  const bool done = __all_sync(0xffffffffu, wait_bar(bar_mma, 0, dev_status));  // warp-uniform for tcgen05.ld
   if (ok && done) {
     tc_fence_after();
     uint32_t v[32];
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(128)
     mma_commit(bar_mma);  // also drains on failure
   }
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  const bool done = wait_bar(bar_mma, 0, dev_status);
+  const bool done = __all_sync(0xffffffffu, wait_bar(bar_mma, 0, dev_status));  // warp-uniform for tcgen05.ld
   if (ok && done) {
     tc_fence_after();
     uint32_t vh[32], vl[32];
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(AM_THREADS, 1)
     mma_commit(bar_mma);  // also drains on failure
   }
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  const bool done = wait_bar(bar_mma, 0, dev_status);
+  const bool done = __all_sync(0xffffffffu, wait_bar(bar_mma, 0, dev_status));  // warp-uniform for tcgen05.ld
   if (warp < 4 && ok && done) {  // TMEM lanes 32 w .. 32 w + 31: warps 0-3
     tc_fence_after();
     uint32_t vh[32], vl[32];

@@ -133,7 +133,8 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(b_q);
-    if (mbar_wait_bounded(b_mma, 0, abort_flag, dev_status, WAIT_NS)) {
+    // warp-uniform, since the TMEM loads are warp-wide instructions
+    if (__all_sync(0xffffffffu, mbar_wait_bounded(b_mma, 0, abort_flag, dev_status, WAIT_NS))) {
       tc_fence_after();
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];

@@ -11,6 +11,9 @@ namespace mla {
 // Shapes the tensor-core kernel is built for (DeepSeek-V2 MLA: 128 heads,
 // 512-wide latent, 64-wide RoPE key, 64-token pages).
 bool tc_decode_supported(int n_h, int d_c, int d_r, int page_size);
+// Test build only (MLA_TEST_HOOKS): when set, the tensor-core decode
+// kernels' page producers issue nothing, so their bounded waits run out.
+extern int g_test_withhold;
 // The latent-split pair kernel (each CTA of a cluster owns half of d_c).
 int tc_split_workers(int sms);
 cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t* block_table,

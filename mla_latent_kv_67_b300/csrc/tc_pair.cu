@@ -140,7 +140,11 @@ static_assert(TM_Q + 288 <= TM_COLS, "score CTA TMEM budget");
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 256, false, true);
+#ifdef MLA_TEST_HOOKS
+constexpr uint64_t WAIT_NS = 20000000ull;  // test build: a withheld item times out in 20 ms
+#else
 constexpr uint64_t WAIT_NS = 2000000000ull;
+#endif
 constexpr uint64_t DRAIN_NS = 100000000ull;
 
 struct Params {
@@ -153,6 +157,7 @@ struct Params {
   int max_pages, num_pages;
   float scale_log2;
   int bt_div;  // new tokens per sequence: query row s uses block-table row s / bt_div
+  int withhold;  // read by the test build only: the score CTA's producer issues nothing
 };
 
 // A sequence's share of a worker's page range.
@@ -325,6 +330,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       uint32_t rk = 0;  // ring items issued
       auto put = [&](const CUtensorMap* map, int y) -> bool {
+#ifdef MLA_TEST_HOOKS
+        if (p.withhold) return false;  // test build: withhold every ring item
+#endif
         const uint32_t st = rk % NKS;
         if (!cx.wait(KEMPTY + st, ((rk / NKS) & 1) ^ 1)) return false;
         mbar_expect_tx(cx.bar(KFULL + st), KSTAGE);
@@ -862,6 +870,7 @@ cudaError_t tc_pair_launch(const void* q_cat, const void* cache, const int32_t* 
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.bt_div = bt_div > 0 ? bt_div : 1;
+  p.withhold = g_test_withhold;
   static unsigned long long smem_done = 0;
   e = set_max_smem_once((const void*)tcp::tc_pair_decode_kernel, (int)tcp::SMEM_BYTES, smem_done);
   if (e != cudaSuccess) return e;

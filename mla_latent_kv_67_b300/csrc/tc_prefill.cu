@@ -307,28 +307,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_try_wait(bar(PFREE + (last & 1)), (last >> 1) & 1);
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
-        if (qi < p.N) {
-          __nv_bfloat16* dst = p.o + ((size_t)qi * NH + h) * DV;
+        // every lane runs the TMEM loads (warp-wide instructions); only rows
+        // inside the prompt store
+        const bool live = qi < p.N;
+        __nv_bfloat16* dst = p.o + ((size_t)(live ? qi : 0) * NH + h) * DV;
 #pragma unroll 1
-          for (int cc = 0; cc < DV / 32; ++cc) {
-            uint32_t v[32];
-            tmem_ld32(lane_base + TM_O + cc * 32, v);
-            tmem_ld_wait();
-            uint32_t pkd[16];
+        for (int cc = 0; cc < DV / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + TM_O + cc * 32, v);
+          tmem_ld_wait();
+          uint32_t pkd[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l);
+          for (int i = 0; i < 16; ++i)
+            pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l);
+          if (live) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               reinterpret_cast<uint4*>(dst + cc * 32)[i] =
                   make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
           }
-          if (p.lse) p.lse[(size_t)qi * NH + h] = (m + log2f(l)) * 0.69314718055994531f;
-        } else {
-          uint32_t v[32];  // keep the warp's TMEM loads uniform
-          tmem_ld32(lane_base + TM_O, v);
-          tmem_ld_wait();
         }
+        if (live && p.lse) p.lse[(size_t)qi * NH + h] = (m + log2f(l)) * 0.69314718055994531f;
       }
     }
   }

@@ -726,7 +726,6 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
   return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int g_withhold = 0;  // set by the test build's mla_test_withhold_pages
 
 // Clusters of two that can be resident at once on the current device with
 // this kernel's shared memory (0 if the query fails). Cached per device.
@@ -774,6 +773,8 @@ int tc_split_workers(int sms) {
   return n;
 }
 
+int g_test_withhold = 0;  // set by the test build's mla_test_withhold_pages
+
 cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t* block_table,
                             int max_pages, int num_pages, int B, int workers, float scale,
                             const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
@@ -795,7 +796,7 @@ cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t*
   p.num_pages = num_pages;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.bt_div = bt_div > 0 ? bt_div : 1;
-  p.withhold = tcs::g_withhold;
+  p.withhold = g_test_withhold;
   static unsigned long long smem_done = 0;
   e = set_max_smem_once((const void*)tcs::tc_split_decode_kernel, (int)tcs::SMEM_BYTES, smem_done);
   if (e != cudaSuccess) return e;
@@ -809,5 +810,5 @@ cudaError_t tc_split_launch(const void* q_cat, const void* cache, const int32_t*
 // Test build only: make the next decode launches' page producer withhold
 // every page, so the bounded waits of both CTAs run out (20 ms in this
 // build) and the kernel reports MLA_DEV_TIMEOUT and returns.
-extern "C" void mla_test_withhold_pages(int on) { mla::tcs::g_withhold = on ? 1 : 0; }
+extern "C" void mla_test_withhold_pages(int on) { mla::g_test_withhold = on ? 1 : 0; }
 #endif

@@ -4,10 +4,11 @@ lets the kernel return, so a lost arrival never hangs the GPU.
 
 The test loads the library's test build (libmla_b300_testhooks.so: the same
 sources with the wait limit cut to 20 ms and mla_test_withhold_pages), makes
-the page producer withhold every page -- before any copy or product is
-issued -- and checks that the call returns, the status word says
-MLA_DEV_TIMEOUT, and a normal decode afterwards in the same process still
-matches the oracle. Nothing faults and nothing is left waiting.
+the page producer of each tensor-core decode kernel withhold every page --
+before any copy or product is issued -- and checks that the call returns,
+the status word says MLA_DEV_TIMEOUT, and a normal decode afterwards in the
+same process still matches the oracle. Nothing faults and nothing is left
+waiting.
 """
 import ctypes
 import time
@@ -34,13 +35,16 @@ def hook_lib():
     return lib
 
 
-def test_withheld_pages_time_out_and_the_next_call_is_correct(monkeypatch):
+@pytest.mark.parametrize("path", [1, 2], ids=["score_value_pair", "latent_split"])
+def test_withheld_pages_time_out_and_the_next_call_is_correct(monkeypatch, path):
     lib = hook_lib()
     monkeypatch.setattr(M, "_lib", lib)  # every binding call goes to the test build
     wl = synth.WORKLOADS["dsv2_b32_ctx4k"].replace(name="timeout", batch=3, lens=(100, 700, 4096),
                                                    seed=31)
+    lib.mla_force_decode_path(path)
     st = DecodeStep(wl)
-    if M.mla_decode_path(st.dtype, st.dims) != 1:
+    if M.mla_decode_path(st.dtype, st.dims) != path:
+        lib.mla_force_decode_path(-1)
         pytest.skip("tensor-core decode kernel not available")
     st.absorb_q()
     st.plan()
@@ -61,6 +65,7 @@ def test_withheld_pages_time_out_and_the_next_call_is_correct(monkeypatch):
     st.run()
     torch.cuda.synchronize()
     assert st.status() == 0, f"status {st.status():#x}"
+    lib.mla_force_decode_path(-1)
     ex = Expected(wl)
     for b in range(wl.batch):
         got = {"o_lat": st.o_lat[b].double().cpu().numpy(), "lse": st.lse[b].double().cpu().numpy(),
