@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-other", action="store_true",
                     help="measure only --workload (skip the other_workloads entries)")
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="override the workload's context length (small cases for profiling)")
     return ap.parse_args()
 
 
@@ -425,7 +427,9 @@ def main():
     mbuild.build()
     from mla_latent_kv_67_b300 import synth
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = synth.WORKLOADS.get(args.workload) or synth.EXTRA_WORKLOADS[args.workload]
+    if args.ctx:
+        wl = wl.replace(name=f"{wl.name}_ctx{args.ctx}", ctx=args.ctx, ctx_range=None, lens=None)
     stream = torch.cuda.current_stream()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
@@ -572,7 +576,7 @@ def main():
             del ost, og
             torch.cuda.empty_cache()
         line["other_workloads"] = others
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl.mode == "attn":
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and wl.mode == "attn" and not args.ctx:
         line["cpu_baseline"] = cpu_baseline_entry(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)
