@@ -96,12 +96,15 @@ def algorithmic(wl, lens):
     two contractions (scores over d_c + d_r, latent output over d_c). With
     q_len new tokens per sequence the rows are still read once, and new
     token t of a sequence of length L attends over L - q_len + 1 + t rows."""
-    esz = 2 if wl.dtype == "bf16" else 4
+    esz = 4 if wl.dtype == "f32" else 2
     lens = np.asarray(lens, np.int64)
     tokens = int(np.sum(lens))
     R = len(lens) * wl.q_len
     seen = int(np.sum(lens)) * wl.q_len - len(lens) * (wl.q_len * (wl.q_len - 1) // 2)
-    cache = tokens * (wl.d_c + wl.d_r) * esz
+    if wl.dtype == "fp8":  # the FP8 row: codes, bf16 RoPE key, scale, padding
+        cache = tokens * ((wl.d_c + 2 * wl.d_r + 4 + 15) // 16 * 16)
+    else:
+        cache = tokens * (wl.d_c + wl.d_r) * esz
     q = R * wl.n_h * (wl.d_c + wl.d_r) * esz
     o = R * wl.n_h * wl.d_c * 4
     flops = seen * (2 * wl.n_h * (wl.d_c + wl.d_r) + 2 * wl.n_h * wl.d_c)
@@ -297,7 +300,7 @@ def run_reference(args):
 # -------------------------------------------------------------------- ours
 def weight_bytes(wl):
     """Bytes of the weights one step of the workload reads (bf16 or fp32)."""
-    esz = 2 if wl.dtype == "bf16" else 4
+    esz = 4 if wl.dtype == "f32" else 2
     if wl.fused:
         k = wl.d_cq or wl.d_model
         n = (wl.d_c + wl.d_r) * wl.d_model + wl.d_cq * wl.d_model   # W^DKV | W^KR, W^DQ
@@ -588,7 +591,8 @@ def main():
 # measured beside the headline workload in the same run (the tiny fp32
 # workload is a parity case only)
 OTHER_WORKLOADS = ("dsv2_b4_ctx128k", "dsv2_b128_ragged", "dsv2_layer_b64_ctx32k",
-                   "dsv2_layer_b64_ctx32k_fused", "dsv2_b32_ctx4k_mtp2", "dsv2_prefill_4k")
+                   "dsv2_layer_b64_ctx32k_fused", "dsv2_b32_ctx4k_mtp2", "dsv2_prefill_4k",
+                   "dsv2_b32_ctx4k_fp8")
 
 
 if __name__ == "__main__":

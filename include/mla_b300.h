@@ -68,7 +68,18 @@ typedef enum {
 #define MLA_DEV_BAD_LEN 0x4     /* sequence length < 1 or past the table     */
 #define MLA_DEV_TIMEOUT 0x8     /* a bounded wait inside a kernel gave up    */
 
-typedef enum { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1, MLA_FP8_E4M3 = 2 } mla_dtype;
+
+/* The FP8 latent cache (MLA_FP8_E4M3, decode only; DeepSeek-V2 MLA page 5.1
+ * item 3 names quantizing the absorbed path): each cached row is
+ *   bytes [0, d_c)               c_KV as E4M3 codes (OCP FP8, max 448)
+ *   bytes [d_c, d_c + 2 d_r)     k_R as bf16 (the RoPE key is kept in bf16)
+ *   bytes [d_c + 2 d_r, +4)      float scale s: c_KV[i] = e4m3(code[i]) * s
+ *   then zeros up to MLA_FP8_ROW_BYTES (a multiple of 16).
+ * The cache argument of mla_decode_attn is then [num_pages][page_size]
+ * [MLA_FP8_ROW_BYTES(d_c, d_r)] bytes; q_cat is bf16, o_lat and lse float;
+ * the plan and workspace are those of dtype MLA_FP8_E4M3. */
+#define MLA_FP8_ROW_BYTES(d_c, d_r) ((((d_c) + 2 * (d_r) + 4) + 15) / 16 * 16)
 
 /* Model dimensions (notation of the DeepSeek-V2 MLA page, 1.1 / 2.1 / 3.2). */
 typedef struct {

@@ -17,7 +17,7 @@ import torch
 from . import build as _build
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA = range(5)
-MLA_F32, MLA_BF16 = 0, 1
+MLA_F32, MLA_BF16, MLA_FP8_E4M3 = 0, 1, 2
 MLA_DEV_BAD_BLOCK, MLA_DEV_BAD_POS, MLA_DEV_BAD_LEN, MLA_DEV_TIMEOUT = 1, 2, 4, 8
 
 LIB_PATH = _build.LIB
@@ -99,6 +99,8 @@ def _dt(t: torch.Tensor) -> int:
         return MLA_F32
     if t.dtype == torch.bfloat16:
         return MLA_BF16
+    if t.dtype == torch.uint8:  # the FP8 latent cache (row format of the header)
+        return MLA_FP8_E4M3
     raise MlaError(MLA_ERR_INVALID_ARG, f"unsupported dtype {t.dtype}")
 
 
@@ -122,7 +124,23 @@ def _stream(stream=None):
 
 
 def torch_dtype(dtype: int):
+    """Element type of the queries, weights and activations for `dtype` (the
+    FP8 cache comes with bf16 everything else)."""
     return torch.float32 if dtype == MLA_F32 else torch.bfloat16
+
+
+def fp8_row_bytes(d_c: int, d_r: int) -> int:
+    """MLA_FP8_ROW_BYTES of the header."""
+    return (d_c + 2 * d_r + 4 + 15) // 16 * 16
+
+
+def _cache_shape(cache, dims: Dims):
+    w = fp8_row_bytes(dims.d_c, dims.d_r) if cache.dtype == torch.uint8 else dims.d_c + dims.d_r
+    return (cache.shape[0], dims.page_size, w)
+
+
+def _q_dtype(cache):
+    return torch.bfloat16 if cache.dtype == torch.uint8 else cache.dtype
 
 
 # ------------------------------------------------------------- entry points
@@ -215,8 +233,8 @@ def mla_decode_attn(q_cat, cache, block_table, seq_lens, scale: float, workspace
     B, max_pages = block_table.shape
     dt = _dt(cache)
     _check(lib().mla_decode_attn(
-        _ptr(q_cat, cache.dtype, (B, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
-        _ptr(cache, shape=(cache.shape[0], dims.page_size, dims.d_c + dims.d_r), name="cache"),
+        _ptr(q_cat, _q_dtype(cache), (B, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
+        _ptr(cache, shape=_cache_shape(cache, dims), name="cache"),
         _ptr(block_table, torch.int32, name="block_table"), max_pages, cache.shape[0],
         _ptr(seq_lens, torch.int32, (B,), "seq_lens"), B, scale,
         _ptr(workspace, torch.uint8, name="workspace"), workspace.numel(),
@@ -242,8 +260,8 @@ def mla_decode_attn_mtp(q_cat, cache, block_table, seq_lens, q_len: int, scale: 
     dt = _dt(cache)
     R = B * q_len
     _check(lib().mla_decode_attn_mtp(
-        _ptr(q_cat, cache.dtype, (R, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
-        _ptr(cache, shape=(cache.shape[0], dims.page_size, dims.d_c + dims.d_r), name="cache"),
+        _ptr(q_cat, _q_dtype(cache), (R, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
+        _ptr(cache, shape=_cache_shape(cache, dims), name="cache"),
         _ptr(block_table, torch.int32, name="block_table"), max_pages, cache.shape[0],
         _ptr(seq_lens, torch.int32, (B,), "seq_lens"), B, q_len, scale,
         _ptr(workspace, torch.uint8, name="workspace"), workspace.numel(),
@@ -297,8 +315,8 @@ def mla_decode_attn_static(q_cat, cache, block_table, seq_lens, scale: float, o_
     B, max_pages = block_table.shape
     dt = _dt(cache)
     _check(lib().mla_decode_attn_static(
-        _ptr(q_cat, cache.dtype, (B, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
-        _ptr(cache, shape=(cache.shape[0], dims.page_size, dims.d_c + dims.d_r), name="cache"),
+        _ptr(q_cat, _q_dtype(cache), (B, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
+        _ptr(cache, shape=_cache_shape(cache, dims), name="cache"),
         _ptr(block_table, torch.int32, name="block_table"), max_pages, cache.shape[0],
         _ptr(seq_lens, torch.int32, (B,), "seq_lens"), B, scale,
         _ptr(o_lat, torch.float32, (B, dims.n_h, dims.d_c), "o_lat"),

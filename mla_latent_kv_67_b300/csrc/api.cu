@@ -68,7 +68,13 @@ mla_status check_dims(const mla_dims* d) {
 }
 
 mla_status check_dtype(int dt) {
-  REQUIRE(dt == MLA_F32 || dt == MLA_BF16, "unknown dtype %d", dt);
+  REQUIRE(dt == MLA_F32 || dt == MLA_BF16,
+          "dtype %d: this call takes MLA_F32 or MLA_BF16 (the FP8 cache is for decode only)", dt);
+  return MLA_OK;
+}
+
+mla_status check_decode_dtype(int dt) {
+  REQUIRE(dt == MLA_F32 || dt == MLA_BF16 || dt == MLA_FP8_E4M3, "unknown dtype %d", dt);
   return MLA_OK;
 }
 
@@ -109,7 +115,8 @@ cudaError_t launch_decode(const DecodeSetup& ds, const void* q_cat, const void* 
                            softmax_scale, ws, ds.L, o_lat, lse, dev_status, ds.q_len, s);
   return launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
                             softmax_scale, ws, ds.L, o_lat, lse, d->n_h, d->d_c, d->d_r,
-                            d->page_size, dtype == MLA_F32, dev_status, ds.q_len, s);
+                            d->page_size, dtype == MLA_F32 ? 1 : (dtype == MLA_FP8_E4M3 ? 2 : 0),
+                            dev_status, ds.q_len, s);
 }
 
 mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* block_table,
@@ -118,7 +125,7 @@ mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* blo
                         const mla_dims* dims, DecodeSetup* out) {
   mla_status st = check_dims(dims);
   if (st != MLA_OK) return st;
-  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  if ((st = check_decode_dtype(dtype)) != MLA_OK) return st;
   REQUIRE(B >= 0, "B must be >= 0");
   REQUIRE(q_len >= 1 && q_len <= MLA_MAX_NEW_TOKENS, "q_len must be in [1, %d] (got %d)",
           MLA_MAX_NEW_TOKENS, q_len);
@@ -159,7 +166,7 @@ void mla_force_decode_path(int path) {
 }
 
 int mla_decode_path(mla_dtype dtype, const mla_dims* dims) {
-  if (check_dims(dims) != MLA_OK || check_dtype(dtype) != MLA_OK) return -1;
+  if (check_dims(dims) != MLA_OK || check_decode_dtype(dtype) != MLA_OK) return -1;
   return pick_path(dtype, dims);
 }
 
@@ -439,7 +446,7 @@ mla_status mla_absorb_q(const void* q, const void* w_uk, void* q_cat, int B, mla
 }
 
 size_t mla_decode_workspace_size(int B, mla_dtype dtype, const mla_dims* dims) {
-  if (check_dims(dims) != MLA_OK || check_dtype(dtype) != MLA_OK || B < 0) return 0;
+  if (check_dims(dims) != MLA_OK || check_decode_dtype(dtype) != MLA_OK || B < 0) return 0;
   const int workers = workers_for(pick_path(dtype, dims));
   if (workers <= 0) return 0;
   return workspace_layout(B, workers, dims->n_h, dims->d_c).total;
@@ -450,7 +457,7 @@ mla_status mla_plan_decode_mtp(const int32_t* seq_lens, int B, int q_len, int ma
                                const mla_dims* dims, int32_t* dev_status, void* stream) {
   mla_status st = check_dims(dims);
   if (st != MLA_OK) return st;
-  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  if ((st = check_decode_dtype(dtype)) != MLA_OK) return st;
   REQUIRE(B >= 0 && max_pages > 0, "B must be >= 0 and max_pages > 0");
   REQUIRE(q_len >= 1 && q_len <= MLA_MAX_NEW_TOKENS, "q_len must be in [1, %d] (got %d)",
           MLA_MAX_NEW_TOKENS, q_len);
@@ -506,7 +513,7 @@ mla_status mla_combine(const void* workspace, size_t ws_bytes, int B, float* o_l
                        mla_dtype dtype, const mla_dims* dims, void* stream) {
   mla_status st = check_dims(dims);
   if (st != MLA_OK) return st;
-  if ((st = check_dtype(dtype)) != MLA_OK) return st;
+  if ((st = check_decode_dtype(dtype)) != MLA_OK) return st;
   REQUIRE(B >= 0, "B must be >= 0");
   if (B == 0) return MLA_OK;
   REQUIRE(o_lat && lse, "NULL tensor argument");

@@ -62,6 +62,8 @@ cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32
                                const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
                                int n_h, int d_c, int d_r, int page_size, int f32,
                                int32_t* dev_status, int bt_div, cudaStream_t s);
+// (f32: 1 = fp32 cache and queries, 0 = bf16, 2 = the FP8 row format with
+// bf16 queries.)
 
 // Plan for B sequences with q_len new tokens each: B * q_len query rows;
 // row v = b * q_len + t sees seq_lens[b] - (q_len - 1 - t) cached tokens.
@@ -75,7 +77,8 @@ mla_status record_error(mla_status st, const char* msg);
 
 // Host-side checks and dispatch shared by the decode entry points (api.cu).
 mla_status check_dims(const mla_dims* d);
-mla_status check_dtype(int dt);
+mla_status check_dtype(int dt);         // MLA_F32 or MLA_BF16
+mla_status check_decode_dtype(int dt);  // also MLA_FP8_E4M3 (the FP8 cache)
 int pick_path(mla_dtype dt, const mla_dims* d);  // 1 tcgen05, 0 SIMT
 int workers_for(int path);                       // workers the plan cuts the pages into
 struct DecodeSetup {

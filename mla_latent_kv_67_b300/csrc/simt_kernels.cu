@@ -3,6 +3,7 @@
 // They serve every dtype/shape the tensor-core kernels do not (the fp32 path,
 // small head counts) and give the tensor-core kernels an independent GPU
 // cross-check. fp32 arithmetic throughout; bf16 operands are widened on load.
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -235,9 +236,30 @@ cudaError_t launch_copy_rope_part(const void* q, void* q_cat, int B, int n_h, in
 // l, l+32, ... (d_c <= 512, d_c % 32 == 0).
 constexpr int SD_HEADS = 8, SD_TOK = 32, SD_MAXC = 16;
 
+// Cache row readers: element k of physical row `row`, widened to float.
 template <typename T>
+struct ElemRows {  // [rows][W] of T (float or bf16)
+  const T* c;
+  int W;
+  __device__ float operator()(long long row, int k) const { return load_elem(c, row * W + k); }
+};
+struct Fp8Rows {  // the FP8 row format of include/mla_b300.h
+  const uint8_t* c;
+  int rb, d_c, d_r;
+  __device__ float operator()(long long row, int k) const {
+    const uint8_t* r = c + row * rb;
+    if (k < d_c) {
+      __nv_fp8_e4m3 v;
+      v.__x = r[k];
+      return static_cast<float>(v) * *reinterpret_cast<const float*>(r + d_c + 2 * d_r);
+    }
+    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(r + d_c)[k - d_c]);
+  }
+};
+
+template <typename T, typename Rows>
 __global__ void __launch_bounds__(256) simt_decode_kernel(
-    const T* __restrict__ q_cat, const T* __restrict__ cache, const int32_t* __restrict__ block_table,
+    const T* __restrict__ q_cat, const Rows cache, const int32_t* __restrict__ block_table,
     int max_pages, int num_pages, int B, float scale, const char* __restrict__ ws, WorkspaceLayout L,
     float* __restrict__ o_lat, float* __restrict__ lse_out, int n_h, int d_c, int d_r,
     int page_size, int32_t* dev_status, int bt_div) {
@@ -245,7 +267,7 @@ __global__ void __launch_bounds__(256) simt_decode_kernel(
   const int W = d_c + d_r, Wp = W + 1;
   float* tile = smem;                     // [SD_TOK][Wp]
   float* qs = tile + SD_TOK * Wp;         // [SD_HEADS][W]
-  __shared__ long long row_off[SD_TOK];   // element offset of each staged row, -1 = skip
+  __shared__ long long row_idx[SD_TOK];   // physical row of each staged token, -1 = skip
 
   const WorkerPlan wp = reinterpret_cast<const WorkerPlan*>(ws + L.workers)[blockIdx.x];
   if (wp.n_pages == 0) return;
@@ -276,20 +298,20 @@ __global__ void __launch_bounds__(256) simt_decode_kernel(
       const int nt = min(SD_TOK, tok1 - t0);
       __syncthreads();
       if (threadIdx.x < SD_TOK) {
-        long long off = -1;
+        long long ri = -1;
         if ((int)threadIdx.x < nt) {
           const int tok = t0 + threadIdx.x;
           const int blk = block_table[(size_t)(s / bt_div) * max_pages + tok / page_size];
           if (blk < 0 || blk >= num_pages) report(dev_status, MLA_DEV_BAD_BLOCK);
-          else off = ((long long)blk * page_size + tok % page_size) * W;
+          else ri = (long long)blk * page_size + tok % page_size;
         }
-        row_off[threadIdx.x] = off;
+        row_idx[threadIdx.x] = ri;
       }
       __syncthreads();
       for (int i = threadIdx.x; i < nt * W; i += blockDim.x) {
         const int r = i / W, k = i % W;
-        const long long off = row_off[r];
-        tile[r * Wp + k] = off >= 0 ? load_elem(cache, off + k) : 0.f;
+        const long long ri = row_idx[r];
+        tile[r * Wp + k] = ri >= 0 ? cache(ri, k) : 0.f;
       }
       __syncthreads();
       if (live) {
@@ -341,6 +363,25 @@ __global__ void __launch_bounds__(256) simt_decode_kernel(
   }
 }
 
+template <typename T, typename Rows>
+static cudaError_t simt_decode_launch(const T* q_cat, const Rows& rows, const int32_t* block_table,
+                                      int max_pages, int num_pages, int B, int workers, float scale,
+                                      const void* ws, const WorkspaceLayout& L, float* o_lat,
+                                      float* lse, int n_h, int d_c, int d_r, int page_size,
+                                      int32_t* dev_status, int bt_div, cudaStream_t s) {
+  const int W = d_c + d_r;
+  const size_t smem = sizeof(float) * ((size_t)SD_TOK * (W + 1) + (size_t)SD_HEADS * W);
+  const dim3 grid(workers, (n_h + SD_HEADS - 1) / SD_HEADS);
+  cudaError_t e = cudaFuncSetAttribute(simt_decode_kernel<T, Rows>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  simt_decode_kernel<T, Rows><<<grid, 256, smem, s>>>(q_cat, rows, block_table, max_pages,
+                                                      num_pages, B, scale, (const char*)ws, L,
+                                                      o_lat, lse, n_h, d_c, d_r, page_size,
+                                                      dev_status, bt_div);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32_t* block_table,
                                int max_pages, int num_pages, int B, int workers, float scale,
                                const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
@@ -348,23 +389,20 @@ cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32
                                int32_t* dev_status, int bt_div, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   const int W = d_c + d_r;
-  const size_t smem = sizeof(float) * ((size_t)SD_TOK * (W + 1) + (size_t)SD_HEADS * W);
-  dim3 grid(workers, (n_h + SD_HEADS - 1) / SD_HEADS);
-  cudaError_t e;
-  if (f32) {
-    e = cudaFuncSetAttribute(simt_decode_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    simt_decode_kernel<float><<<grid, 256, smem, s>>>(
-        (const float*)q_cat, (const float*)cache, block_table, max_pages, num_pages, B, scale,
-        (const char*)ws, L, o_lat, lse, n_h, d_c, d_r, page_size, dev_status, bt_div);
-  } else {
-    e = cudaFuncSetAttribute(simt_decode_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    simt_decode_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(
-        (const __nv_bfloat16*)q_cat, (const __nv_bfloat16*)cache, block_table, max_pages, num_pages,
-        B, scale, (const char*)ws, L, o_lat, lse, n_h, d_c, d_r, page_size, dev_status, bt_div);
-  }
-  return cudaGetLastError();
+  if (f32 == 1)
+    return simt_decode_launch((const float*)q_cat, ElemRows<float>{(const float*)cache, W},
+                              block_table, max_pages, num_pages, B, workers, scale, ws, L, o_lat,
+                              lse, n_h, d_c, d_r, page_size, dev_status, bt_div, s);
+  if (f32 == 0)
+    return simt_decode_launch((const __nv_bfloat16*)q_cat,
+                              ElemRows<__nv_bfloat16>{(const __nv_bfloat16*)cache, W}, block_table,
+                              max_pages, num_pages, B, workers, scale, ws, L, o_lat, lse, n_h, d_c,
+                              d_r, page_size, dev_status, bt_div, s);
+  // FP8 latent cache, bf16 queries
+  const Fp8Rows rows{(const uint8_t*)cache, MLA_FP8_ROW_BYTES(d_c, d_r), d_c, d_r};
+  return simt_decode_launch((const __nv_bfloat16*)q_cat, rows, block_table, max_pages, num_pages,
+                            B, workers, scale, ws, L, o_lat, lse, n_h, d_c, d_r, page_size,
+                            dev_status, bt_div, s);
 }
 
 }  // namespace mla

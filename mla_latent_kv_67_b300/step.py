@@ -36,7 +36,7 @@ class DecodeStep:
     def __init__(self, wl: synth.Workload, device="cuda", out_dtype=None):
         self.wl, self.device = wl, torch.device(device)
         self.dims = M.Dims.of(wl)
-        self.dtype = M.MLA_BF16 if wl.dtype == "bf16" else M.MLA_F32
+        self.dtype = {"bf16": M.MLA_BF16, "f32": M.MLA_F32, "fp8": M.MLA_FP8_E4M3}[wl.dtype]
         tdt = M.torch_dtype(self.dtype)
         dev = self.device
         lens = synth.seq_lens(wl)
@@ -90,6 +90,7 @@ class DecodeStep:
         else:
             self.q = to_device(synth.storage(wl, synth.query(wl)), wl, dev)
         assert wl.q_len == 1 or wl.mode == "attn", "several new tokens: attention-only workloads"
+        assert wl.dtype != "fp8" or wl.mode == "attn", "the FP8 cache: attention-only workloads"
         if wl.mode == "prefill_mha":
             N = wl.ctx
             self.rows = torch.empty((N, wl.d_c + wl.d_r), dtype=tdt, device=dev)

@@ -11,6 +11,10 @@ Value recipe (stated once, used everywhere):
 * token hidden states ``x`` ~ N(0, 1);
 * bf16 workloads round every drawn value to bf16 (round-to-nearest-even) once,
   here, so both sides see exactly the same numbers;
+* fp8 workloads store the cache's latent part as E4M3 codes with one float
+  scale per row (scale = max |c| / 448, codes = c / scale rounded to the
+  nearest E4M3 value, ties to even) and its RoPE part in bf16; everything
+  else is bf16. Both sides see the decoded values code * scale;
 * context lengths are either fixed or uniform integers in ``[lo, hi]``
   (inclusive);
 * the physical page pool is a seeded random permutation of all logical pages
@@ -115,6 +119,9 @@ WORKLOADS: dict[str, Workload] = {
 EXTRA_WORKLOADS: dict[str, Workload] = {
     "dsv2_b32_ctx4k_mtp2": Workload(name="dsv2_b32_ctx4k_mtp2", batch=32, ctx=4096, q_len=2,
                                     seed=67006),
+    # the batch-32, 4096-token decode over an FP8 latent cache
+    "dsv2_b32_ctx4k_fp8": Workload(name="dsv2_b32_ctx4k_fp8", batch=32, ctx=4096, dtype="fp8",
+                                   seed=67008),
     "dsv2_layer_b64_ctx32k_fused": WORKLOADS["dsv2_layer_b64_ctx32k"].replace(
         name="dsv2_layer_b64_ctx32k_fused", fused=True),
     # a 4096-token prompt prefilled in the MHA form (DeepSeek-V2 shapes)
@@ -148,12 +155,74 @@ def _draw(wl: Workload, g: np.random.Generator, shape, std: float = 1.0) -> np.n
     v = g.standard_normal(shape, dtype=np.float32)
     if std != 1.0:
         v *= np.float32(std)
-    return round_bf16(v) if wl.dtype == "bf16" else v
+    return round_bf16(v) if wl.dtype in ("bf16", "fp8") else v
 
 
 def storage(wl: Workload, a: np.ndarray) -> np.ndarray:
-    """Device storage form of float32 values: uint16 bf16 bits or float32."""
-    return bf16_bits(a) if wl.dtype == "bf16" else np.ascontiguousarray(a, np.float32)
+    """Device storage form of float32 values: uint16 bf16 bits or float32
+    (fp8 workloads keep everything but the cache in bf16)."""
+    if wl.dtype in ("bf16", "fp8"):
+        return bf16_bits(a)
+    return np.ascontiguousarray(a, np.float32)
+
+
+# ------------------------------------------------------------ E4M3 format
+def _e4m3_table() -> np.ndarray:
+    """Value of every E4M3 code (OCP FP8: 1 sign, 4 exponent bits with bias
+    7, 3 mantissa bits; exponent 0 is subnormal; 0x7F / 0xFF are NaN)."""
+    out = np.empty(256, np.float64)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        e, m = (code >> 3) & 0xF, code & 0x7
+        if e == 15 and m == 7:
+            out[code] = np.nan
+        elif e == 0:
+            out[code] = sign * (m / 8.0) * 2.0 ** -6
+        else:
+            out[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return out
+
+
+E4M3 = _e4m3_table()
+E4M3_MAX = 448.0
+
+
+def e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """float32 -> the nearest finite E4M3 code (ties to the even code),
+    magnitudes past 448 clamped to 448."""
+    x = np.asarray(x, np.float32)
+    a = np.abs(x).astype(np.float64)
+    pos = E4M3[:127]                          # codes 0x00 .. 0x7E, ascending
+    idx = np.clip(np.searchsorted(pos, a), 1, 126)
+    lo, hi = pos[idx - 1], pos[idx]
+    up = (a - lo > hi - a) | ((a - lo == hi - a) & (idx % 2 == 0))
+    code = np.where(up, idx, idx - 1)
+    code = np.where(a >= E4M3_MAX, 126, code).astype(np.uint8)
+    return code | np.where(np.signbit(x), np.uint8(0x80), np.uint8(0))
+
+
+def fp8_row_bytes(d_c: int, d_r: int) -> int:
+    return (d_c + 2 * d_r + 4 + 15) // 16 * 16
+
+
+def fp8_rows(wl: Workload, rows: np.ndarray):
+    """float32 cache rows [n][d_c + d_r] -> (the FP8 row bytes [n][row_bytes],
+    the values they decode to, float32 [n][d_c + d_r])."""
+    rows = np.asarray(rows, np.float32)
+    c, k = rows[:, :wl.d_c], rows[:, wl.d_c:]
+    amax = np.max(np.abs(c), axis=1)
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    codes = e4m3_codes(c / s[:, None])
+    dec = np.empty_like(rows)
+    dec[:, :wl.d_c] = E4M3[codes].astype(np.float32) * s[:, None]
+    kb = bf16_bits(k)
+    dec[:, wl.d_c:] = bf16_to_f32(kb)
+    rb = fp8_row_bytes(wl.d_c, wl.d_r)
+    out = np.zeros((rows.shape[0], rb), np.uint8)
+    out[:, :wl.d_c] = codes
+    out[:, wl.d_c:wl.d_c + 2 * wl.d_r] = kb.view(np.uint8).reshape(rows.shape[0], -1)
+    out[:, wl.d_c + 2 * wl.d_r:wl.d_c + 2 * wl.d_r + 4] = s.view(np.uint8).reshape(-1, 4)
+    return out, dec
 
 
 # ---------------------------------------------------------- lengths / paging
@@ -191,7 +260,12 @@ def block_table(wl: Workload, lens: np.ndarray) -> tuple[np.ndarray, int]:
 
 
 def cache_page(wl: Workload, b: int, p: int) -> np.ndarray:
-    """Logical page ``p`` of sequence ``b``: float32 ``[page_size][d_c+d_r]``."""
+    """Logical page ``p`` of sequence ``b``: float32 ``[page_size][d_c+d_r]``
+    (for fp8 workloads the values the stored FP8 rows decode to)."""
+    if wl.dtype == "fp8":
+        raw = _rng(wl, _S_CACHE, b, p).standard_normal((wl.page_size, wl.row_width),
+                                                       dtype=np.float32)
+        return fp8_rows(wl, raw)[1]
     return _draw(wl, _rng(wl, _S_CACHE, b, p), (wl.page_size, wl.row_width))
 
 
@@ -222,6 +296,8 @@ def paged_cache(wl: Workload, lens: np.ndarray, bt: np.ndarray, pool: int) -> np
     step, rows past a sequence's end and unmapped pages hold ``PAD_VALUE``."""
     P, W = wl.page_size, wl.row_width
     pad = np.float32(PAD_VALUE)
+    if wl.dtype == "fp8":
+        return _paged_cache_fp8(wl, lens, bt, pool)
     out = np.empty((pool, P, W), dtype=np.uint16 if wl.dtype == "bf16" else np.float32)
     out[...] = storage(wl, np.full((1,), pad, np.float32))[0]
     nd = drawn_rows(wl, lens)
@@ -234,6 +310,25 @@ def paged_cache(wl: Workload, lens: np.ndarray, bt: np.ndarray, pool: int) -> np
                 page = page.copy()
                 page[keep:] = pad
             out[bt[b, p]] = storage(wl, page)
+    return out
+
+
+def _paged_cache_fp8(wl: Workload, lens, bt, pool) -> np.ndarray:
+    """The FP8 page pool ``[pool][page_size][row_bytes]`` (attention-only
+    workloads: every owned row drawn; other rows encode PAD_VALUE)."""
+    P, W = wl.page_size, wl.row_width
+    pad_row = fp8_rows(wl, np.full((1, W), PAD_VALUE, np.float32))[0][0]
+    out = np.empty((pool, P, fp8_row_bytes(wl.d_c, wl.d_r)), np.uint8)
+    out[...] = pad_row
+    nd = drawn_rows(wl, lens)
+    for b in range(wl.batch):
+        n = int(nd[b])
+        for p in range((n + P - 1) // P):
+            raw = _rng(wl, _S_CACHE, b, p).standard_normal((P, W), dtype=np.float32)
+            enc = fp8_rows(wl, raw)[0]
+            keep = min(P, n - p * P)
+            page = out[bt[b, p]]
+            page[:keep] = enc[:keep]
     return out
 
 

@@ -53,3 +53,31 @@ def test_layer_mode_leaves_append_slot_padded():
         p, r = divmod(129, 64)
         assert np.all(cache[bt[b, p], r] == synth.PAD_VALUE)
         assert np.array_equal(cache[bt[b, 0]], synth.cache_page(wl, b, 0))
+
+
+def test_e4m3_format_and_fp8_rows():
+    """The E4M3 codes of the FP8 cache: the format's fixed points (448 the
+    largest finite value, 2^-9 the smallest subnormal, 2^-6 the smallest
+    normal, 0x7F not a number), every finite value encodes to itself, ties go
+    to the even code, magnitudes past 448 clamp; a row decodes to its codes
+    times its scale and its bf16 RoPE part."""
+    import numpy as np
+    from mla_latent_kv_67_b300 import synth
+    t = synth.E4M3
+    assert t[0x7E] == 448.0 and t[0x01] == 2.0 ** -9 and t[0x08] == 2.0 ** -6 and np.isnan(t[0x7F])
+    assert t[0xBE] == -448.0 and t[0x38] == 1.0
+    finite = np.array([c for c in range(256) if not np.isnan(t[c]) and c != 0x80], np.uint8)
+    assert np.array_equal(synth.e4m3_codes(t[finite].astype(np.float32)), finite)
+    # 1.0625 lies halfway between 1.0 (0x38) and 1.125 (0x39): even code 0x38;
+    # 1.1875 halfway between 1.125 (0x39) and 1.25 (0x3A): 0x3A
+    got = synth.e4m3_codes(np.array([1.0625, 1.1875, 1e9, -1e9], np.float32))
+    assert list(got) == [0x38, 0x3A, 0x7E, 0xFE]
+    wl = synth.EXTRA_WORKLOADS["dsv2_b32_ctx4k_fp8"]
+    rows = np.random.default_rng(3).standard_normal((5, wl.row_width)).astype(np.float32)
+    enc, dec = synth.fp8_rows(wl, rows)
+    assert enc.shape == (5, synth.fp8_row_bytes(wl.d_c, wl.d_r)) and enc.shape[1] % 16 == 0
+    s = enc[:, wl.d_c + 2 * wl.d_r:wl.d_c + 2 * wl.d_r + 4].copy().view(np.float32)[:, 0]
+    assert np.array_equal(dec[:, :wl.d_c], t[enc[:, :wl.d_c]].astype(np.float32) * s[:, None])
+    assert np.max(np.abs(dec[:, :wl.d_c])) <= 448.0 * s.max()
+    assert np.allclose(dec[:, :wl.d_c], rows[:, :wl.d_c], rtol=2.0 ** -4, atol=2.0 ** -9 * s.max())
+    assert np.array_equal(dec[:, wl.d_c:], synth.round_bf16(rows[:, wl.d_c:]))
