@@ -65,7 +65,7 @@ def test_e4m3_format_and_fp8_rows():
     from mla_latent_kv_67_b300 import synth
     t = synth.E4M3
     assert t[0x7E] == 448.0 and t[0x01] == 2.0 ** -9 and t[0x08] == 2.0 ** -6 and np.isnan(t[0x7F])
-    assert t[0xBE] == -448.0 and t[0x38] == 1.0
+    assert t[0xFE] == -448.0 and t[0x38] == 1.0
     finite = np.array([c for c in range(256) if not np.isnan(t[c]) and c != 0x80], np.uint8)
     assert np.array_equal(synth.e4m3_codes(t[finite].astype(np.float32)), finite)
     # 1.0625 lies halfway between 1.0 (0x38) and 1.125 (0x39): even code 0x38;
