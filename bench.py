@@ -53,7 +53,7 @@ DEFAULT_WORKLOAD = "dsv2_b32_ctx4k"
 # the capture measured: drop the entry whenever the decode kernel changes,
 # until it is captured again.
 DECODE_TRAFFIC = {}
-DECODE_KERNELS = {0: "simt", 1: "tcgen05 latent-split pair", 2: "tcgen05 score/value pair"}
+DECODE_KERNELS = {0: "simt", 1: "tcgen05 score/value pair", 2: "tcgen05 latent-split pair"}
 
 
 def parse():
