@@ -13,7 +13,8 @@
 //   v      [N][n_h][d_v]         = c W^UV_h^T
 //   o_i,h  = sum_{j <= i} softmax_j(q_i,h . [k_nope_j,h ; k_R,j] * scale) v_j,h
 //
-// One CTA per (head, 128-query tile), the heaviest tiles (most keys) first.
+// One CTA per (head, 128-query tile); heads in groups of eight, the heaviest
+// tiles (most keys) of a group first.
 // Per 128-key tile: S = Q . K^T (M = 128 queries, N = 128 keys, K = 192)
 // into one of two TMEM buffers, online softmax by four warps (thread = query
 // row = TMEM lane; lazy rescale of O: only when a row maximum grows by more
@@ -35,6 +36,8 @@ namespace tpf {
 using namespace ptx;
 
 constexpr int NH = 128, DH = 128, DR = 64, DC = 512, DV = 128, QW = DH + DR, ROW = DC + DR;
+constexpr int HG = 8;  // heads per scheduling group
+static_assert(NH % HG == 0, "head groups");
 constexpr int TQ = 128, TK = 128;          // queries / keys per tile
 constexpr uint32_t CH = 128 * 128;         // one 64-column chunk of a 128-row tile: 16 KB
 constexpr int NQC = QW / 64;               // Q chunks: 3 (two no-PE, one RoPE)
@@ -95,9 +98,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest query tiles (most key tiles) first
-  const int h = blockIdx.x % NH;
-  const int qt = p.n_qt - 1 - (int)(blockIdx.x / NH);
+  // Heads in groups of HG; within a group the heaviest query tiles (most key
+  // tiles) first. The CTAs in flight then share the keys of a few heads,
+  // which stay in L2, instead of touching the keys of every head at once.
+  const int grp = (int)blockIdx.x / (HG * p.n_qt), r = (int)blockIdx.x % (HG * p.n_qt);
+  const int h = grp * HG + r % HG;
+  const int qt = p.n_qt - 1 - r / HG;
   const int q0 = qt * TQ;
   const int nkt = qt + 1;  // key tiles 0 .. qt
 
