@@ -470,7 +470,7 @@ mla_status mla_plan_decode_mtp(const int32_t* seq_lens, int B, int q_len, int ma
   if (!workspace || ws_bytes < L.total)
     return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L.total);
   return cuda_status(launch_plan(seq_lens, B, q_len, max_pages, dims->page_size, workers, path,
-                                 workspace, L, dev_status, S(stream)),
+                                 dtype != MLA_F32, workspace, L, dev_status, S(stream)),
                      "plan_decode");
 }
 

@@ -19,6 +19,14 @@ __device__ __forceinline__ void store_elem(__nv_bfloat16* p, size_t i, float v) 
   p[i] = __float2bfloat16_rn(v);
 }
 
+// Four consecutive bf16 partial elements starting at element e (e a
+// multiple of 4) of a bf16 array at byte address base, as floats.
+__device__ __forceinline__ float4 load_part_bf16x4(const char* base, size_t e) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(base) + e / 4);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
 __device__ __forceinline__ void report(int32_t* dev_status, int bits) {
   if (dev_status) atomicOr(dev_status, bits);
 }
@@ -28,15 +36,19 @@ __device__ __forceinline__ void report(int32_t* dev_status, int bits) {
 // `workers` contiguous ranges of `per_worker` pages. Worker g owns global
 // pages [g*per, min((g+1)*per, total)). A sequence touched by k > 1 workers
 // owns k partial slots starting at `slot_begin`; its k-th worker (in order)
-// writes slot slot_begin + k.
+// writes slot slot_begin + k. A slot is the normalised partial output
+// [n_h][d_c] (element ((slot * n_h + h) * d_c + c) of the o_part region, in
+// bf16 when the header's part_bf16 is set, else fp32) and its lse [n_h]
+// (fp32).
 struct PlanHeader {
   int32_t workers;      // number of workers the plan was made for
   int32_t per_worker;   // cost units per worker (>= 1)
   int32_t total_pages;  // sum over sequences
   int32_t num_slots;    // partial slots used
   int32_t batch;
-  int32_t path;         // decode kernel the plan is for (0 SIMT, 1 tcgen05)
-  int32_t pad[2];
+  int32_t path;         // decode kernel the plan is for (0 SIMT, 1 and 2 tcgen05)
+  int32_t part_bf16;    // partial slots hold bf16 (bf16 / FP8 caches) or fp32 (fp32 cache)
+  int32_t pad;
 };
 
 struct SeqPlan {

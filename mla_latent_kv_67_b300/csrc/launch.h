@@ -67,8 +67,10 @@ cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32
 
 // Plan for B sequences with q_len new tokens each: B * q_len query rows;
 // row v = b * q_len + t sees seq_lens[b] - (q_len - 1 - t) cached tokens.
+// part_bf16: the decode kernels keep split partials in bf16 (bf16 and FP8
+// caches) rather than fp32 (fp32 cache); the combine reads it from the plan.
 cudaError_t launch_plan(const int32_t* seq_lens, int B, int q_len, int max_pages, int page_size,
-                        int workers, int path, void* ws, const WorkspaceLayout& L,
+                        int workers, int path, bool part_bf16, void* ws, const WorkspaceLayout& L,
                         int32_t* dev_status, cudaStream_t s);
 cudaError_t launch_combine(const void* ws, const WorkspaceLayout& L, int B, int n_h, int d_c,
                            float* o_lat, float* lse, cudaStream_t s);

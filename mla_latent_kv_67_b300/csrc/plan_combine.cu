@@ -46,8 +46,8 @@ constexpr int PLAN_SMEM_SEQS = 4096;  // sequences whose cost prefix stays in sh
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ seq_lens, int B,
                                                     int q_len, int max_pages, int page_size,
                                                     int workers,
-                                                    int path, int c_seg, char* ws, WorkspaceLayout L,
-                                                    int32_t* dev_status) {
+                                                    int path, int part_bf16, int c_seg, char* ws,
+                                                    WorkspaceLayout L, int32_t* dev_status) {
   __shared__ int warp_sums[32];
   __shared__ int carry_s, ccarry_s;
   __shared__ int vend_s[PLAN_SMEM_SEQS], pages_s[PLAN_SMEM_SEQS];
@@ -175,30 +175,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     hdr->num_slots = num_slots;
     hdr->batch = B;
     hdr->path = path;
+    hdr->part_bf16 = part_bf16;
   }
 }
 
 // One warp per (sequence, head), four heads per block: merge the sequence's
 // partial slots, o = sum_s exp(lse_s - lse) o_s with lse = log sum_s
 // exp(lse_s). Each lane owns float4 columns lane, lane + 32, ... so every
-// load and store of the warp is one contiguous row piece.
-__global__ void __launch_bounds__(128) combine_kernel(const char* __restrict__ ws, WorkspaceLayout L,
-                                                      int n_h, int d_c, float* __restrict__ o_lat,
-                                                      float* __restrict__ lse) {
-  const int b = blockIdx.x;
-  const int h = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (h >= n_h) return;
-  const SeqPlan sp = reinterpret_cast<const SeqPlan*>(ws + L.seqs)[b];
-  if (sp.n_splits == 1) return;  // written by the decode kernel
+// load and store of the warp is one contiguous row piece. P16: the partial
+// slots hold bf16 (else fp32).
+template <bool P16>
+__device__ __forceinline__ void merge_row(const char* __restrict__ ws, const WorkspaceLayout& L,
+                                          const SeqPlan& sp, int b, int h, int lane, int n_h,
+                                          int d_c, float* __restrict__ o_lat,
+                                          float* __restrict__ lse) {
   float4* o = reinterpret_cast<float4*>(o_lat + ((size_t)b * n_h + h) * d_c);
   const int n4 = d_c / 4;
-  if (sp.n_splits == 0) {  // invalid length: defined, empty result
-    for (int i = lane; i < n4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane == 0) lse[(size_t)b * n_h + h] = -INFINITY;
-    return;
-  }
   const float* lp = reinterpret_cast<const float*>(ws + L.lse_part);
-  const float* op = reinterpret_cast<const float*>(ws + L.o_part);
   const int n = sp.n_splits;
   constexpr int MAXV = 4;  // float4 columns per lane held in registers (d_c <= 512)
   constexpr int RS = 4;    // splits whose rows are loaded per round
@@ -209,11 +202,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const char* __restrict__ w
 #pragma unroll
     for (int t = 0; t < RS; ++t) {
       const size_t slot = (size_t)(sp.slot_begin + min(s0 + t, n - 1));
-      const float4* src = reinterpret_cast<const float4*>(op + (slot * n_h + h) * d_c);
+      const size_t e0 = (slot * n_h + h) * d_c;
 #pragma unroll
       for (int v = 0; v < MAXV; ++v) {
         const int i = lane + 32 * v;
-        x[t][v] = i < n4 ? ptx::ld_nc_v4(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i >= n4)
+          x[t][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        else if (P16)
+          x[t][v] = load_part_bf16x4(ws + L.o_part, e0 + 4 * (size_t)i);
+        else
+          x[t][v] = ptx::ld_nc_v4(
+              reinterpret_cast<const float4*>(reinterpret_cast<const float*>(ws + L.o_part) + e0) + i);
       }
     }
   };
@@ -262,14 +261,34 @@ __global__ void __launch_bounds__(128) combine_kernel(const char* __restrict__ w
   if (lane == 0) lse[(size_t)b * n_h + h] = m + logf(z);
 }
 
+
+__global__ void __launch_bounds__(128) combine_kernel(const char* __restrict__ ws, WorkspaceLayout L,
+                                                      int n_h, int d_c, float* __restrict__ o_lat,
+                                                      float* __restrict__ lse) {
+  const int b = blockIdx.x;
+  const int h = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (h >= n_h) return;
+  const SeqPlan sp = reinterpret_cast<const SeqPlan*>(ws + L.seqs)[b];
+  const bool p16 = reinterpret_cast<const PlanHeader*>(ws + L.header)->part_bf16 != 0;
+  if (sp.n_splits == 1) return;  // written by the decode kernel
+  if (sp.n_splits == 0) {        // invalid length: defined, empty result
+    float4* o = reinterpret_cast<float4*>(o_lat + ((size_t)b * n_h + h) * d_c);
+    for (int i = lane; i < d_c / 4; i += 32) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) lse[(size_t)b * n_h + h] = -INFINITY;
+    return;
+  }
+  if (p16) merge_row<true>(ws, L, sp, b, h, lane, n_h, d_c, o_lat, lse);
+  else merge_row<false>(ws, L, sp, b, h, lane, n_h, d_c, o_lat, lse);
+}
+
 cudaError_t launch_plan(const int32_t* seq_lens, int B, int q_len, int max_pages, int page_size,
-                        int workers, int path, void* ws, const WorkspaceLayout& L,
+                        int workers, int path, bool part_bf16, void* ws, const WorkspaceLayout& L,
                         int32_t* dev_status, cudaStream_t s) {
   // the tcgen05 kernel's per-sequence cost (Q fetch, O write-out) is worth
   // about four pages; the SIMT kernel's is small next to its page cost
   const int c_seg = path >= 1 ? 4 : 0;
   plan_kernel<<<1, 1024, 0, s>>>(seq_lens, B * q_len, q_len, max_pages, page_size, workers, path,
-                                 c_seg, (char*)ws, L, dev_status);
+                                 part_bf16 ? 1 : 0, c_seg, (char*)ws, L, dev_status);
   return cudaGetLastError();
 }
 

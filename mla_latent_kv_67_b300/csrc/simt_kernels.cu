@@ -344,20 +344,24 @@ __global__ void __launch_bounds__(256) simt_decode_kernel(
       }
     }
     if (live) {
-      float* dst;
+      const float inv = 1.f / l;
       float* lse_dst;
       if (sp.n_splits == 1) {
-        dst = o_lat + ((size_t)s * n_h + h) * d_c;
+        float* dst = o_lat + ((size_t)s * n_h + h) * d_c;
         lse_dst = lse_out + (size_t)s * n_h + h;
-      } else {
-        const int slot = sp.slot_begin + (blockIdx.x - sp.first_worker);
-        dst = reinterpret_cast<float*>(const_cast<char*>(ws) + L.o_part) + ((size_t)slot * n_h + h) * d_c;
-        lse_dst = reinterpret_cast<float*>(const_cast<char*>(ws) + L.lse_part) + (size_t)slot * n_h + h;
-      }
-      const float inv = 1.f / l;
 #pragma unroll
-      for (int i = 0; i < SD_MAXC; ++i)
-        if (i < ncol) dst[lane + 32 * i] = acc[i] * inv;
+        for (int i = 0; i < SD_MAXC; ++i)
+          if (i < ncol) dst[lane + 32 * i] = acc[i] * inv;
+      } else {
+        // a split partial: bf16 for bf16 / FP8 caches, fp32 for fp32
+        const int slot = sp.slot_begin + (blockIdx.x - sp.first_worker);
+        const size_t e0 = ((size_t)slot * n_h + h) * d_c;
+        char* op = const_cast<char*>(ws) + L.o_part;
+        lse_dst = reinterpret_cast<float*>(const_cast<char*>(ws) + L.lse_part) + (size_t)slot * n_h + h;
+#pragma unroll
+        for (int i = 0; i < SD_MAXC; ++i)
+          if (i < ncol) store_elem(reinterpret_cast<T*>(op), e0 + lane + 32 * i, acc[i] * inv);
+      }
       if (lane == 0) *lse_dst = m + logf(l);
     }
   }

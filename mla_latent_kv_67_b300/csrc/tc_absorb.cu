@@ -285,6 +285,7 @@ __global__ void __launch_bounds__(AM_THREADS, 1)
   const SeqPlan* seqs = reinterpret_cast<const SeqPlan*>(ws + L.seqs);
   const float* lp = reinterpret_cast<const float*>(ws + L.lse_part);
   const float* op = reinterpret_cast<const float*>(ws + L.o_part);
+  const bool p16 = reinterpret_cast<const PlanHeader*>(ws + L.header)->part_bf16 != 0;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_w);
@@ -325,20 +326,23 @@ __global__ void __launch_bounds__(AM_THREADS, 1)
     // round 0 of both rows: a split past the end re-reads the last one
     // (weight 0); an unsplit row reads its o_lat row (weight 1)
     float4 x[2][RS][4];
-    auto src_of = [&](int k, int sidx) -> const float4* {
-      if (n[k] >= 2)
-        return reinterpret_cast<const float4*>(
-            op + ((size_t)(sbeg[k] + min(sidx, n[k] - 1)) * NH + h) * DC);
-      return reinterpret_cast<const float4*>(o_lat + ((size_t)bb[k] * NH + h) * DC);
+    // float4 column lane + 32 q of split sidx of row k (partials in bf16 or
+    // fp32 as the plan says), or of the row's o_lat if it was not split
+    auto ld = [&](int k, int sidx, int q) -> float4 {
+      const int c4 = lane + 32 * q;
+      if (n[k] >= 2) {
+        const size_t e0 = ((size_t)(sbeg[k] + min(sidx, n[k] - 1)) * NH + h) * DC;
+        return p16 ? load_part_bf16x4(ws + L.o_part, e0 + 4 * (size_t)c4)
+                   : ld_nc_v4(reinterpret_cast<const float4*>(op + e0) + c4);
+      }
+      return ld_nc_v4(reinterpret_cast<const float4*>(o_lat + ((size_t)bb[k] * NH + h) * DC) + c4);
     };
 #pragma unroll
     for (int k = 0; k < 2; ++k)
 #pragma unroll
-      for (int t = 0; t < RS; ++t) {
-        const float4* src = src_of(k, t);
+      for (int t = 0; t < RS; ++t)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) x[k][t][q] = ld_nc_v4(src + lane + 32 * q);
-      }
+        for (int q = 0; q < 4; ++q) x[k][t][q] = ld(k, t, q);
     float l_lane[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k)
@@ -372,11 +376,9 @@ __global__ void __launch_bounds__(AM_THREADS, 1)
         for (int s0 = 0; s0 < nk; s0 += RS) {
           if (s0 > 0) {  // later rounds (more than RS splits)
 #pragma unroll
-            for (int t = 0; t < RS; ++t) {
-              const float4* src = src_of(k, s0 + t);
+            for (int t = 0; t < RS; ++t)
 #pragma unroll
-              for (int q = 0; q < 4; ++q) x[k][t][q] = ld_nc_v4(src + lane + 32 * q);
-            }
+              for (int q = 0; q < 4; ++q) x[k][t][q] = ld(k, s0 + t, q);
           }
 #pragma unroll
           for (int t = 0; t < RS; ++t) {

@@ -14,10 +14,14 @@
 // products therefore run on the two CTAs (two SMs) of a cluster, each once:
 //
 //   rank 0, the score CTA: Q_cat in TMEM as the A operand, S into TMEM
-//     (three buffers), pages from a 3-stage ring; two MMA issuer threads
-//     take even and odd pages (one issuer alone cannot keep the tensor core
-//     busy with 64-wide products); four softmax warps
-//     (thread = head row = TMEM lane) turn S into bf16 probabilities P and
+//     (three buffers), pages from a 3-stage ring; three MMA issuer threads
+//     take pages in turn (page i into S buffer i % 3). A page's 36 products
+//     all accumulate into one S buffer, so each waits for the one before:
+//     one such chain keeps the tensor core about a third busy at N = 64, and
+//     three chains in flight are needed to fill it. Two groups of four
+//     softmax warps take the pages in turn (thread = head row = TMEM lane;
+//     the groups share each page's reference maximum through shared
+//     memory) and turn S into bf16 probabilities P and
 //     store them, with per-row rescale factors, straight from registers into
 //     the value CTA's shared memory (st.async, completion counted in bytes on
 //     the value CTA's barrier). A sequence's Q_cat rows (128 x 576, the same
@@ -72,6 +76,8 @@ constexpr int NKS = 3;                  // score CTA: page stages
 constexpr int NVS = 2;                  // value CTA: latent page stages
 constexpr int NP = 3;                   // P slots
 constexpr int NSB = 3;                  // S buffers in TMEM
+constexpr int NQK = 3;                  // QK issuer threads (page i: issuer and S buffer i % 3)
+static_assert(NQK == NSB, "each QK issuer owns one S buffer");
 constexpr uint32_t KSTAGE = NCHUNK * CHUNK;
 constexpr int HALF_BLOCKS = DC / 2 / 32;  // 32-column TMEM blocks in one half of O
 constexpr uint32_t VSTAGE = VCHUNK * CHUNK;
@@ -87,7 +93,12 @@ constexpr uint32_t P_TX = P_BYTES + X_BYTES;  // bytes that fill one P slot
 
 // score CTA shared memory
 constexpr uint32_t S_OFF_K = 0;
-constexpr uint32_t S_OFF_BAR = S_OFF_K + NKS * KSTAGE;
+// the two softmax groups' hand-over: the reference maximum each page used
+// ([2][NH], by page parity), and at a sequence's end the l and reference of
+// the group that does not own the last page ([2][NH] each)
+constexpr uint32_t S_OFF_MREF = S_OFF_K + NKS * KSTAGE;
+constexpr uint32_t S_OFF_LX = S_OFF_MREF + 2 * NH * 4;
+constexpr uint32_t S_OFF_BAR = S_OFF_LX + 4 * NH * 4;
 enum {
   KFULL = 0,             // [NKS] ring item (page or Q half) landed
   KEMPTY = NKS,          // [NKS] ring item consumed (4 arrivals)
@@ -96,9 +107,10 @@ enum {
   QTMEM = SFREE + NSB,   // Q of the segment in TMEM (4 warps)
   QEMPTY = QTMEM + 1,    // last QK of a segment done
   PEMPTY = QEMPTY + 1,   // [NP] value CTA done with P slot (its PV commit)
-  SFINAL = PEMPTY + NP,  // drain after an abort (issuer 0)
-  SFINAL2 = SFINAL + 1,  // drain after an abort (issuer 1)
-  S_NBAR = SFINAL2 + 1
+  SFINAL = PEMPTY + NP,  // [NQK] drain after an abort (one per QK issuer)
+  MREADY = SFINAL + 3,   // [2] reference maximum of a page published (4 warps), by page parity
+  LXREADY = MREADY + 2,  // [2] l of the non-last group published at a sequence's end (4 warps)
+  S_NBAR = LXREADY + 2
 };
 constexpr uint32_t S_OFF_TSLOT = S_OFF_BAR + 8 * S_NBAR;
 constexpr uint32_t S_OFF_ABORT = S_OFF_TSLOT + 4;
@@ -248,7 +260,7 @@ __device__ __forceinline__ bool for_each_page(const Params& p, const WorkerPlan&
   return ok;
 }
 
-constexpr int THREADS = 320;
+constexpr int THREADS = 384;
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_pair_decode_kernel(const __grid_constant__ CUtensorMap tm_cache,
@@ -284,9 +296,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       for (int i = 0; i < NP; ++i) mbar_init(cx.bar(PEMPTY + i), 1);
       mbar_init(cx.bar(QTMEM), 4);
-      mbar_init(cx.bar(QEMPTY), 2);  // one commit per QK issuer
-      mbar_init(cx.bar(SFINAL), 1);
-      mbar_init(cx.bar(SFINAL2), 1);
+      mbar_init(cx.bar(QEMPTY), NQK);  // one commit per QK issuer
+      for (int i = 0; i < NQK; ++i) mbar_init(cx.bar(SFINAL + i), 1);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(cx.bar(MREADY + i), 4);
+        mbar_init(cx.bar(LXREADY + i), 4);
+      }
     } else {
       for (int i = 0; i < NVS; ++i) {
         mbar_init(cx.bar(VFULL + i), 1);
@@ -348,16 +363,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (uint32_t k = rk > (uint32_t)NKS ? rk - NKS : 0; k < rk; ++k)
           mbar_wait_drain(cx.bar(KFULL + k % NKS), (k / NKS) & 1, DRAIN_NS);
       }
-    } else if (warp == 1 || warp == 6) {
+    } else if (warp == 1 || warp == 6 || warp == 7) {
       // --------------------------------------------------------- QK issue
-      // issuer e = 0 (warp 1) takes even pages into S0, e = 1 (warp 6) odd
-      // pages into S1. Both wait for every sequence's Q (so neither can fall
-      // a phase behind) and arrive once per sequence on QEMPTY: by a commit
+      // issuer e (warps 1, 6, 7) takes the pages with it % 3 == e, into S
+      // buffer e. Each waits for every sequence's Q (so none can fall a
+      // phase behind) and arrives once per sequence on QEMPTY: by a commit
       // after its last QK of the sequence, or a plain arrive if it had none
       // (a commit with no new MMA since the thread's previous commit does not
       // arrive).
       if (lane == 0) {
-        const uint32_t e = warp == 1 ? 0u : 1u;
+        const uint32_t e = warp == 1 ? 0u : warp == 6 ? 1u : 2u;
         uint32_t it = 0, seg = 0;
         bool ok = true;
         for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
@@ -367,7 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ok = cx.wait(QTMEM, seg & 1);
           bool issued = false;
           for (int j = 0; ok && j < n; ++j, ++it) {
-            if ((it & 1) != e) continue;
+            if (it % NQK != e) continue;
             const uint32_t rk = it + 2 * (seg + 1);  // ring item: two Q halves per sequence so far
             const uint32_t st = rk % NKS, sb = it % NSB;
             ok = cx.wait(SFREE + sb, ((it / NSB) & 1) ^ 1) && cx.wait(KFULL + st, (rk / NKS) & 1);
@@ -395,8 +410,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           mbar_wait_drain(cx.bar(SFINAL + e), 0, DRAIN_NS);
         }
       }
-    } else if (warp >= 2 && warp <= 5) {
+    } else if ((warp >= 2 && warp <= 5) || (warp >= 8 && warp <= 11)) {
       // ---------------------------------------------------------- softmax
+      // Two groups of four warps (G = 0: warps 2-5, G = 1: warps 8-11) take
+      // the pages in turn, page it by group it % 2, so one group's
+      // exponentials and P stores overlap the other's. Both use the same
+      // reference maximum for every page: the group of page it reads the
+      // reference page it - 1 used (published in shared memory) before it
+      // fixes its own (the lazy rescale rule). Each group keeps l over its own
+      // pages; at a sequence's end the group of the last page adds the other
+      // group's l, brought to the final reference.
+      const int G = warp >= 8 ? 1 : 0;
       const int q4 = warp & 3;
       const int row = q4 * 32 + lane;
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -405,6 +429,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t peer_x0 = mapa_shared(sbase + V_OFF_X, peer);
       float* lse_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.lse_part);
       const float c = p.scale_log2;
+      float* mref = reinterpret_cast<float*>(smem + S_OFF_MREF);  // [2][NH]
+      float* lxl = reinterpret_cast<float*>(smem + S_OFF_LX);     // [2][NH] l
+      float* lxm = lxl + 2 * NH;                                  // [2][NH] its reference
       // This thread's Q_cat row from ring item rq (rows 0-63) or rq + 1
       // (rows 64-127), un-swizzled, into TMEM columns [TM_Q, TM_Q + 288);
       // the item's two warps then release it.
@@ -435,17 +462,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         return true;
       };
-      uint32_t it = 0, seg = 0;
+      uint32_t it = 0, seg = 0, nlx = 0;  // nlx: sequences so far with two or more pages
       Seg sg;
       bool have = next_seg(w, seqs, g, w.seq_begin, sg);
-      bool ok = !have || load_q(0);
+      bool ok = !have || G == 1 || load_q(0);
       for (; ok && have; ++seg) {
         Seg nx;
         const bool have_next = next_seg(w, seqs, g, sg.s + 1, nx);
-        float m = -INFINITY, l = 0.f;
         const int n = sg.p1 - sg.p0;
         const uint32_t rq_next = it + n + 2 * (seg + 1);  // ring item of the next sequence's Q
+        float m_own = 0.f, l = 0.f;  // this group's last reference and its l relative to it
+        bool mine = false;
         for (int j = 0; j < n; ++j, ++it) {
+          if ((int)(it & 1u) != G) continue;
           const uint32_t sb = it % NSB;
           ok = __all_sync(0xffffffffu, cx.wait(SFULL + sb, (it / NSB) & 1));
           if (!ok) break;
@@ -475,15 +504,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             mx[3] = fmaxf(mx[3], __uint_as_float(sc[i + 1]));
           }
           const float mp = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c;
-          float m_use = m, alpha = 1.f;
+          // reference maximum of this page: the page maximum on a sequence's
+          // first page, else the previous page's reference unless this page's
+          // maximum exceeds it by more than 8 (then O is rescaled by alpha)
+          float m_use = mp, alpha = 1.f;
           bool resc = false;
-          if (j == 0) {
-            m_use = mp;
-          } else if (mp > m + 8.f) {
-            m_use = mp;
-            alpha = ex2_approx(m - mp);
-            resc = true;
+          if (j > 0) {
+            const uint32_t pi = it - 1;  // the other group's page
+            ok = __all_sync(0xffffffffu, cx.wait(MREADY + (pi & 1), (pi >> 1) & 1));
+            if (!ok) break;
+            const float m_prev = mref[(pi & 1) * NH + row];
+            if (mp > m_prev + 8.f) {
+              alpha = ex2_approx(m_prev - mp);
+              resc = true;
+            } else {
+              m_use = m_prev;
+            }
           }
+          mref[(it & 1) * NH + row] = m_use;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(cx.bar(MREADY + (it & 1)));
+
           const float nm = -m_use;
           float sm[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[32];
@@ -501,9 +542,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             pk[16 + i] = pack_bf16x2(e2, e3);
           }
           const float sum = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-          l = (j == 0) ? sum : fmaf(l, alpha, sum);
-          m = m_use;
+          // the references only grow, so the factor is at most 1
+          l = mine ? fmaf(l, ex2_approx(m_own - m_use), sum) : sum;
+          m_own = m_use;
+          mine = true;
           const bool last = j == n - 1;
+          float inv_l = 0.f, lse = 0.f;
+          if (last) {
+            float lt = l;
+            if (n >= 2) {  // the other group's pages of this sequence
+              ok = __all_sync(0xffffffffu, cx.wait(LXREADY + (nlx & 1), (nlx >> 1) & 1));
+              if (!ok) break;
+              lt = fmaf(lxl[(nlx & 1) * NH + row], ex2_approx(lxm[(nlx & 1) * NH + row] - m_use), l);
+            }
+            inv_l = 1.f / lt;
+            lse = (m_use + log2f(lt)) * 0.69314718055994531f;
+          } else if (j == n - 2) {  // this group's last page of the sequence
+            lxl[(nlx & 1) * NH + row] = l;
+            lxm[(nlx & 1) * NH + row] = m_use;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cx.bar(LXREADY + (nlx & 1)));
+          }
 
           // P row (and the row's rescale factor, 1 / l on the last page)
           // straight into P slot it % NP of the value CTA
@@ -518,9 +577,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         pf);
           const uint32_t px = peer_x0 + slot * X_BYTES;
           st_async_b32(px + XOFF_ALPHA + 4 * row, __float_as_uint(alpha), pf);
-          st_async_b32(px + XOFF_INVL + 4 * row, __float_as_uint(last ? 1.f / l : 0.f), pf);
+          st_async_b32(px + XOFF_INVL + 4 * row, __float_as_uint(inv_l), pf);
           const bool any_resc = __any_sync(0xffffffffu, resc);
           if (lane == 0) st_async_b32(px + XOFF_FLAG + 4 * q4, any_resc ? 1u : 0u, pf);
+          if (last) {
+            if (sg.slot < 0) p.lse[(size_t)sg.s * NH + row] = lse;
+            else lse_part[(size_t)sg.slot * NH + row] = lse;
+          }
 
           // the next sequence's Q as soon as this one's last QK is done (the
           // QK of its first page then overlaps the softmax of this last page)
@@ -533,9 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
         }
         if (!ok) break;
-        const float lse = (m + log2f(l)) * 0.69314718055994531f;
-        if (sg.slot < 0) p.lse[(size_t)sg.s * NH + row] = lse;
-        else lse_part[(size_t)sg.slot * NH + row] = lse;
+        if (n >= 2) ++nlx;
         sg = nx;
         have = have_next;
       }
@@ -550,11 +611,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     auto write_half = [&](const Seg& sg, int half, float inv_l) {
       const int q4 = warp & 3;
       const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)half * (DC / 2);
-      float* o_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.o_part);
-      float* dst0 = (sg.slot < 0 ? p.o_lat + (size_t)sg.s * NH * DC
-                                 : o_part + (size_t)sg.slot * NH * DC) +
-                    half * (DC / 2);
       uint8_t* stg = smem + V_OFF_STG + (warp - 2) * 32 * 128;
+      if (sg.slot >= 0) {
+        // a split partial, in bf16: per two 32-column blocks the thread of
+        // row r parks its 64 values (128 bytes) in the staging tile, then
+        // each store instruction writes 4 whole 128-byte row pieces
+        __nv_bfloat16* d16 = reinterpret_cast<__nv_bfloat16*>(const_cast<char*>(p.ws) + p.L.o_part) +
+                             (size_t)sg.slot * NH * DC + half * (DC / 2);
+#pragma unroll 1
+        for (int cc = 0; cc < HALF_BLOCKS; cc += 2) {
+          uint32_t va[32], vb[32];
+          tmem_ld32(lane_base + cc * 32, va);
+          tmem_ld32(lane_base + (cc + 1) * 32, vb);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t* v = (u < 4 ? va : vb) + 8 * (u & 3);
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((u ^ (lane & 7)) << 4)) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[0]) * inv_l, __uint_as_float(v[1]) * inv_l),
+                pack_bf16x2(__uint_as_float(v[2]) * inv_l, __uint_as_float(v[3]) * inv_l),
+                pack_bf16x2(__uint_as_float(v[4]) * inv_l, __uint_as_float(v[5]) * inv_l),
+                pack_bf16x2(__uint_as_float(v[6]) * inv_l, __uint_as_float(v[7]) * inv_l));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3), u = lane & 7;
+            const uint4 x = *reinterpret_cast<const uint4*>(stg + r * 128 + ((u ^ (r & 7)) << 4));
+            *reinterpret_cast<uint4*>(d16 + (size_t)(q4 * 32 + r) * DC + cc * 32 + 8 * u) = x;
+          }
+          __syncwarp();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cx.bar(OFREE + half));
+        return;
+      }
+      // the final o_lat of an unsplit sequence, in fp32
+      float* dst0 = p.o_lat + (size_t)sg.s * NH * DC + half * (DC / 2);
       auto put_block = [&](int cc, const uint32_t (&v)[32]) {
 #pragma unroll
         for (int u = 0; u < 8; ++u)

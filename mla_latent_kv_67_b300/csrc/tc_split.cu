@@ -636,7 +636,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int row = q4 * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q4 * 32) << 16);
     const float* lbuf = reinterpret_cast<const float*>(smem + OFF_L);
-    float* o_part = reinterpret_cast<float*>(const_cast<char*>(p.ws) + p.L.o_part);
+    __nv_bfloat16* o_part = reinterpret_cast<__nv_bfloat16*>(const_cast<char*>(p.ws) + p.L.o_part);
     uint32_t seg = 0;
     bool ok = true;
     for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
@@ -649,9 +649,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const float inv_l = lbuf[(seg & 1) * NH + row];
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(LFREE + (seg & 1)));
-      float* dst = (sg.slot < 0 ? p.o_lat + (size_t)sg.s * NH * DC
-                                : o_part + (size_t)sg.slot * NH * DC) +
-                   (size_t)row * DC + HALF * rank;
+      // the final o_lat row (fp32) of an unsplit sequence, else the bf16
+      // partial slot
+      const bool part = sg.slot >= 0;
+      float* dst = p.o_lat + ((size_t)sg.s * NH + row) * DC + HALF * rank;
+      __nv_bfloat16* d16 = o_part + ((size_t)(part ? sg.slot : 0) * NH + row) * DC + HALF * rank;
+      auto put8 = [&](int col, const float (&v)[8]) {
+        if (part)
+          *reinterpret_cast<uint4*>(d16 + col) =
+              make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                         pack_bf16x2(v[6], v[7]));
+        else
+          stg_v8(dst + col, v);
+      };
       uint32_t va[32], vb[32];
       tmem_ld32(lane_base + TM_O, va);
 #pragma unroll 1
@@ -663,7 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           float v[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(va[8 * q + e]) * inv_l;
-          stg_v8(dst + cc * 32 + 8 * q, v);
+          put8(cc * 32 + 8 * q, v);
         }
         tmem_ld_wait();
         if (cc + 2 < HALF / 32) tmem_ld32(lane_base + TM_O + (cc + 2) * 32, va);
@@ -672,7 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           float v[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(vb[8 * q + e]) * inv_l;
-          stg_v8(dst + (cc + 1) * 32 + 8 * q, v);
+          put8((cc + 1) * 32 + 8 * q, v);
         }
       }
       tc_fence_before();

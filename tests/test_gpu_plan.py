@@ -45,6 +45,8 @@ def check(lens, max_pages):
     workers, per, total, num_slots, batch = (int(x) for x in hdr[:5])
     B = len(lens)
     assert batch == B
+    assert int(hdr[5]) == path
+    assert int(hdr[6]) == 1  # a bf16 cache keeps its split partials in bf16
     valid = [1 <= n <= max_pages * PAGE for n in lens]
     assert (status != 0) == (not all(valid))
     pages = [(n + PAGE - 1) // PAGE if ok else 0 for n, ok in zip(lens, valid)]
