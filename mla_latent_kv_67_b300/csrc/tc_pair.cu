@@ -101,8 +101,8 @@ constexpr uint32_t S_OFF_LX = S_OFF_MREF + 2 * NH * 4;
 constexpr uint32_t S_OFF_BAR = S_OFF_LX + 4 * NH * 4;
 enum {
   KFULL = 0,             // [NKS] ring item (page or Q half) landed
-  KEMPTY = NKS,          // [NKS][NCHUNK] a 64-column chunk of a ring item consumed (2 arrivals)
-  SFULL = KEMPTY + NKS * NCHUNK,  // [NSB] S buffer written
+  KEMPTY = NKS,          // [NKS] ring item consumed (4 arrivals)
+  SFULL = 2 * NKS,       // [NSB] S buffer written
   SFREE = SFULL + NSB,   // [NSB] S buffer read by the 4 softmax warps
   QTMEM = SFREE + NSB,   // Q of the segment in TMEM (4 warps)
   QEMPTY = QTMEM + 1,    // last QK of a segment done
@@ -288,8 +288,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (rank == 0) {
       for (int i = 0; i < NKS; ++i) {
         mbar_init(cx.bar(KFULL + i), 1);
-        // per chunk: a page's QK issuer arrives and commits; a Q half's two warps arrive
-        for (int c = 0; c < NCHUNK; ++c) mbar_init(cx.bar(KEMPTY + i * NCHUNK + c), 2);
+        mbar_init(cx.bar(KEMPTY + i), 4);  // page: 3 + the QK commit; Q half: 2 warps x 2
       }
       for (int i = 0; i < NSB; ++i) {
         mbar_init(cx.bar(SFULL + i), 1);
@@ -349,23 +348,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #ifdef MLA_TEST_HOOKS
         if (p.withhold) return false;  // test build: withhold every ring item
 #endif
-        // chunk by chunk, each as soon as the same chunk of the item three
-        // back has been consumed; the one arrive comes after every chunk's
-        // byte count (also after an abort, so the issued chunks still
-        // complete the phase the drain below waits for)
-        const uint32_t st = rk % NKS, par = ((rk / NKS) & 1) ^ 1;
-        bool ok = true;
-        for (int c = 0; c < NCHUNK; ++c) {
-          if (!cx.wait(KEMPTY + st * NCHUNK + c, par)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx_only(cx.bar(KFULL + st), CHUNK);
+        const uint32_t st = rk % NKS;
+        if (!cx.wait(KEMPTY + st, ((rk / NKS) & 1) ^ 1)) return false;
+        mbar_expect_tx(cx.bar(KFULL + st), KSTAGE);
+        for (int c = 0; c < NCHUNK; ++c)
           tma_load_2d(sbase + S_OFF_K + st * KSTAGE + c * CHUNK, map, c * 64, y, cx.bar(KFULL + st));
-        }
-        mbar_arrive(cx.bar(KFULL + st));
         ++rk;
-        return ok;
+        return true;
       };
       const bool ok = for_each_page(
           p, w, seqs, g, lane, [&](uint32_t, int bk) -> bool { return put(&tm_cache, bk * PAGE); },
@@ -400,17 +389,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t pg = sbase + S_OFF_K + st * KSTAGE;
-            // chunk c of the page is released once its four products are done
 #pragma unroll
-            for (int c = 0; c < NCHUNK; ++c) {
-#pragma unroll
-              for (int kq = 0; kq < 4; ++kq)
-                mma_ts(tmem + TM_S + sb * 64, tmem + TM_Q + (4 * c + kq) * 8,
-                       sdesc_sw128(pg + c * CHUNK + kq * 32, 16, 1024), IDESC_QK,
-                       (c | kq) > 0 ? 1u : 0u);
-              mbar_arrive(cx.bar(KEMPTY + st * NCHUNK + c));
-              mma_commit(cx.bar(KEMPTY + st * NCHUNK + c));
-            }
+            for (int kk = 0; kk < 4 * NCHUNK; ++kk)
+              mma_ts(tmem + TM_S + sb * 64, tmem + TM_Q + kk * 8,
+                     sdesc_sw128(pg + (kk >> 2) * CHUNK + (kk & 3) * 32, 16, 1024), IDESC_QK,
+                     kk > 0 ? 1u : 0u);
+            mbar_arrive_cnt(cx.bar(KEMPTY + st), 3);  // the commit brings the fourth
+            mma_commit(cx.bar(KEMPTY + st));
             mma_commit(cx.bar(SFULL + sb));
             issued = true;
           }
@@ -466,14 +451,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             v[4 * u + 2] = x.z;
             v[4 * u + 3] = x.w;
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(cx.bar(KEMPTY + st * NCHUNK + c));  // chunk read
           tmem_st32(lane_base + TM_Q + c * 32, v);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(cx.bar(QTMEM));
+        if (lane == 0) {
+          mbar_arrive_cnt(cx.bar(KEMPTY + st), 2);
+          mbar_arrive(cx.bar(QTMEM));
+        }
         return true;
       };
       uint32_t it = 0, seg = 0, nlx = 0;  // nlx: sequences so far with two or more pages
