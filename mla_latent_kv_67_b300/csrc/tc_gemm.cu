@@ -47,6 +47,7 @@ constexpr uint64_t DRAIN_NS = 100000000ull;
 struct Args {
   int M, N, K;
   int mt;   // token rows per tile (multiple of 16, <= MAX_MT)
+  int m_tiles;  // token tiles
   int cs;   // CTAs per cluster splitting K (1, 2, 4 or 8)
   int nst;  // ring stages
   int epi;  // Epilogue (launch.h)
@@ -74,8 +75,13 @@ __global__ void __launch_bounds__(THREADS)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cs = a.cs, mt = a.mt, nst = a.nst;
   const uint32_t rank = cs > 1 ? cluster_ctarank() : 0u;
-  const int n0 = (int)(blockIdx.x / cs) * TILE_N;
-  const int m0 = (int)blockIdx.y * mt;
+  // Tiles in launch order with the token tiles fastest: the CTAs in flight
+  // share a few weight tiles (each read from HBM about once, the rest from
+  // L2) rather than every weight tile at once. A cluster is cs consecutive
+  // blocks of one row of the grid, so all its CTAs get the same tile.
+  const int tile = (int)((blockIdx.y * gridDim.x + blockIdx.x) / (unsigned)cs);
+  const int n0 = (tile / a.m_tiles) * TILE_N;
+  const int m0 = (tile % a.m_tiles) * mt;
   const int nc = a.K / 64;
   const int c0 = (int)(rank * nc / cs), c1 = (int)((rank + 1) * nc / cs);
   const uint32_t SB = stage_bytes(mt);
@@ -164,6 +170,75 @@ __global__ void __launch_bounds__(THREADS)
   if (waited) mbar_try_wait(done, 0);  // each lane acquires the completed phase
   const bool mma_ok = __all_sync(0xffffffffu, waited && !*abort_flag);
   tc_fence_after();
+  if (cs == 1) {
+    // The whole K range is in this CTA's accumulator: thread r (TMEM lane r)
+    // holds output feature n0 + r for every token of the tile, so it reads
+    // 16 tokens at a time from TMEM and, token by token, the warp writes 32
+    // consecutive features (one contiguous piece of the output row).
+    const int r = threadIdx.x, gn = n0 + r;
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    int rk = -1;  // RoPE pair of this feature (-1: none) and its side
+    bool odd = false;
+    if (a.epi == EPI_ROPE || a.epi == EPI_APPEND) {
+      const int col = a.epi == EPI_ROPE ? gn % a.rope_period : gn;
+      if (col >= a.rope_off && col < a.rope_off + a.d_r) {
+        rk = (col - a.rope_off) >> 1;
+        odd = ((col - a.rope_off) & 1) != 0;
+      }
+    }
+    for (int j0 = 0; j0 < mt; j0 += 16) {
+      uint32_t v[16];
+      if (mma_ok) {
+        tmem_ld16(taddr + j0, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v[u] = 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int gm = m0 + j0 + u;
+        float x = __uint_as_float(v[u]);
+        const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
+        if (gm >= a.M || !mma_ok) continue;
+        if (rk >= 0) {
+          const int ps = a.pos[gm];
+          if (ps < 0 || ps >= a.max_pos) {
+            report(a.dev_status, MLA_DEV_BAD_POS);
+          } else {
+            const float2 cs2 = reinterpret_cast<const float2*>(a.rope)[(size_t)ps * (a.d_r / 2) + rk];
+            x = odd ? partner * cs2.y + x * cs2.x : x * cs2.x - partner * cs2.y;
+          }
+        }
+        size_t o;
+        if (a.epi == EPI_APPEND) {
+          const int sq = a.seq_idx ? a.seq_idx[gm] : gm;
+          const int ps = a.pos[gm];
+          if (sq < 0 || sq >= a.B || ps < 0 || ps >= a.max_pages * a.page_size) {
+            report(a.dev_status, MLA_DEV_BAD_POS);
+            continue;
+          }
+          const int blk = a.block_table[(size_t)sq * a.max_pages + ps / a.page_size];
+          if (blk < 0 || blk >= a.num_pages) {
+            report(a.dev_status, MLA_DEV_BAD_BLOCK);
+            continue;
+          }
+          o = ((size_t)blk * a.page_size + ps % a.page_size) * (size_t)a.N + gn;
+        } else {
+          o = (size_t)gm * (size_t)a.ldo + gn;
+        }
+        if (gn >= a.N) continue;
+        if (a.out_f32) reinterpret_cast<float*>(a.out)[o] = x;
+        else reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(x);
+      }
+    }
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, tcols);
+    }
+    return;
+  }
   const int R = TILE_N / cs;  // output features each CTA of the cluster owns
   float* red = reinterpret_cast<float*>(smem);  // [cs][mt][R], reuses the ring
   if (cs > 1) cluster_sync_all();
@@ -303,7 +378,7 @@ cudaError_t tc_gemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s) {
          n_tiles * m_tiles * cs < sms)
     cs *= 2;
   Args a;
-  a.M = M; a.N = N; a.K = K; a.mt = mt; a.cs = cs;
+  a.M = M; a.N = N; a.K = K; a.mt = mt; a.cs = cs; a.m_tiles = m_tiles;
   const uint32_t SB = W_CHUNK + (uint32_t)mt * 128u;
   a.nst = (int)(RING_BYTES / SB);
   if (a.nst > 8) a.nst = 8;

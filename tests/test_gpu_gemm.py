@@ -4,8 +4,9 @@ and mla_out_proj, through the C ABI.
 Each product is checked against a float64 product of the same bf16 values
 (fp32 accumulation on the GPU: max |gpu - ref| / max |ref| <= 1e-5 before
 the output rounding), across shapes that exercise one and several token
-tiles, a ragged last weight tile, and each cluster split of K; the RoPE and
-paged-store epilogues against the oracle.
+tiles (in the order the kernel assigns them), a ragged last weight tile, and
+each cluster split of K; the RoPE and paged-store epilogues against the
+oracle.
 """
 import numpy as np
 import pytest
@@ -31,6 +32,8 @@ OUT_PROJ_SHAPES = [
     (3, 2, 32, 200),        # K = 64 (one chunk), ragged N
     (130, 12, 128, 1000),   # two token tiles, K = 1536
     (257, 1, 64, 96),       # three token tiles, K = 64
+    (600, 4, 128, 384),     # five token tiles, ragged last, K = 512
+    (512, 8, 64, 256),      # four full token tiles x two weight tiles
 ]
 
 
