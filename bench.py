@@ -544,10 +544,13 @@ def main():
 
     roof = dict(res["roofline"])
     roof["kernel_us"] = kernel_ms * 1e3
-    roof["achieved"] = roof["alg_bytes"] / (kernel_ms * 1e-3) / 1e9
-    roof["frac"] = roof["achieved"] / hbm
     roof["tensor_tflops"] = roof["alg_flops"] / (kernel_ms * 1e-3) / 1e12
     roof["tensor_frac"] = roof["tensor_tflops"] / tflops
+    if roof["bound"] == "tensor":  # the kernel's own bound decides the unit
+        roof["achieved"], roof["frac"] = roof["tensor_tflops"], roof["tensor_frac"]
+    else:
+        roof["achieved"] = roof["alg_bytes"] / (kernel_ms * 1e-3) / 1e9
+        roof["frac"] = roof["achieved"] / hbm
     roof["frac_of_roofline"] = roof["roofline_us"] / (kernel_ms * 1e3)
     roof["peak_source"] = peak_kind
     roof["timing"] = "decode launch alone in its own CUDA graph, L2 flushed before each"
