@@ -21,8 +21,9 @@
 // than 8 in log2 units, P and l using the same stale maximum), P as bf16 into
 // TMEM, O += P . V (M = 128, N = d_v = 128, K = 128 keys). The diagonal tile
 // masks keys after the query. Warp 0 streams the key/value tiles with TMA
-// (two stages), warp 1 issues the MMAs. Every wait is bounded and reports
-// MLA_DEV_TIMEOUT.
+// (two stages; a stage's keys are refilled once its S is done, its values
+// once its PV is done, so the next keys do not wait for the PV), warp 1
+// issues the MMAs. Every wait is bounded and reports MLA_DEV_TIMEOUT.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -48,9 +49,10 @@ constexpr int NST = 2;
 constexpr uint32_t OFF_K = OFF_Q + NQC * CH;
 enum {
   QFULL = 0,
-  KFULL = 1,            // [NST]
-  KEMPTY = KFULL + NST, // [NST] the tile's PV done (commit)
-  SFULL = KEMPTY + NST, // [2]
+  KFULL = 1,            // [NST] the tile's keys landed
+  VFULL = KFULL + NST,  // [NST] the tile's values landed
+  VEMPTY = VFULL + NST, // [NST] the tile's PV done (commit); its S done is SFULL
+  SFULL = VEMPTY + NST, // [2]
   SFREE = SFULL + 2,    // [2] (4 warps)
   PFULL = SFREE + 2,    // [2] (4 warps)
   PFREE = PFULL + 2,    // [2] (commit)
@@ -111,7 +113,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(bar(QFULL), 1);
     for (int i = 0; i < NST; ++i) {
       mbar_init(bar(KFULL + i), 1);
-      mbar_init(bar(KEMPTY + i), 1);
+      mbar_init(bar(VFULL + i), 1);
+      mbar_init(bar(VEMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(SFULL + i), 1);
@@ -140,23 +143,42 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tm_v);
     mbar_expect_tx(bar(QFULL), NQC * CH);
     for (int c = 0; c < NQC; ++c) tma_load_3d(sb + OFF_Q + c * CH, &tm_q, 64 * c, h, q0, bar(QFULL));
-    int issued = 0;
+    // A stage's keys and values are refilled separately: the keys of tile
+    // kt + 2 as soon as S of tile kt is done, the values once its PV is
+    // done. Keys run one tile ahead of values: K(kt + 1), then V(kt).
+    int k_issued = 0, v_issued = 0;
     bool ok = true;
-    for (int kt = 0; kt < nkt; ++kt) {
+    auto load_k = [&](int kt) -> bool {
       const int st = kt % NST;
-      ok = wait1(bar(KEMPTY + st), ((kt / NST) & 1) ^ 1, abort_flag, p.dev_status);
-      if (!ok) break;
+      if (kt >= NST && !wait1(bar(SFULL + (kt & 1)), ((kt - NST) >> 1) & 1, abort_flag, p.dev_status))
+        return false;
       const uint32_t dst = sb + OFF_K + st * KSTAGE;
-      mbar_expect_tx(bar(KFULL + st), KSTAGE);
+      mbar_expect_tx(bar(KFULL + st), NQC * CH);
       tma_load_3d(dst, &tm_k, 0, h, kt * TK, bar(KFULL + st));
       tma_load_3d(dst + CH, &tm_k, 64, h, kt * TK, bar(KFULL + st));
       tma_load_2d(dst + 2 * CH, &tm_kr, DC, kt * TK, bar(KFULL + st));
-      tma_load_3d(dst + 3 * CH, &tm_v, 0, h, kt * TK, bar(KFULL + st));
-      tma_load_3d(dst + 4 * CH, &tm_v, 64, h, kt * TK, bar(KFULL + st));
-      issued = kt + 1;
+      k_issued = kt + 1;
+      return true;
+    };
+    auto load_v = [&](int kt) -> bool {
+      const int st = kt % NST;
+      if (!wait1(bar(VEMPTY + st), ((kt / NST) & 1) ^ 1, abort_flag, p.dev_status)) return false;
+      const uint32_t dst = sb + OFF_K + st * KSTAGE + NQC * CH;
+      mbar_expect_tx(bar(VFULL + st), NVC * CH);
+      tma_load_3d(dst, &tm_v, 0, h, kt * TK, bar(VFULL + st));
+      tma_load_3d(dst + CH, &tm_v, 64, h, kt * TK, bar(VFULL + st));
+      v_issued = kt + 1;
+      return true;
+    };
+    ok = load_k(0);
+    for (int kt = 0; ok && kt < nkt; ++kt) {
+      if (kt + 1 < nkt) ok = load_k(kt + 1);
+      if (ok) ok = load_v(kt);
     }
-    for (int i = issued > NST ? issued - NST : 0; i < issued; ++i)
+    for (int i = k_issued > NST ? k_issued - NST : 0; i < k_issued; ++i)
       mbar_wait_drain(bar(KFULL + i % NST), (i / NST) & 1, DRAIN_NS);
+    for (int i = v_issued > NST ? v_issued - NST : 0; i < v_issued; ++i)
+      mbar_wait_drain(bar(VFULL + i % NST), (i / NST) & 1, DRAIN_NS);
     mbar_wait_drain(bar(QFULL), 0, DRAIN_NS);
   } else if (warp == 1 && lane == 0) {
     // ----------------------------------------------------------- MMA issue
@@ -165,15 +187,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool any = false;
     auto pv = [&](int kt) -> bool {
       const int st = kt % NST, pb = kt & 1;
-      if (!wait1(bar(PFULL + pb), (kt >> 1) & 1, abort_flag, p.dev_status)) return false;
+      if (!wait1(bar(PFULL + pb), (kt >> 1) & 1, abort_flag, p.dev_status) ||
+          !wait1(bar(VFULL + st), (kt / NST) & 1, abort_flag, p.dev_status))
+        return false;
       tc_fence_after();
-      const uint32_t vt = sb + OFF_K + st * KSTAGE + 3 * CH;
+      const uint32_t vt = sb + OFF_K + st * KSTAGE + NQC * CH;
 #pragma unroll
       for (int kk = 0; kk < TK / 16; ++kk)
         mma_ts(tmem + TM_O, tmem + TM_P + pb * 64 + kk * 8, sdesc_sw128(vt + kk * 2048, CH, 1024),
                IDESC_PV, (kt > 0 || kk > 0) ? 1u : 0u);
       mma_commit(bar(PFREE + pb));
-      mma_commit(bar(KEMPTY + st));
+      mma_commit(bar(VEMPTY + st));
       return true;
     };
     for (int kt = 0; ok && kt < nkt; ++kt) {
