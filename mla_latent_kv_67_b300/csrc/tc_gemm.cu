@@ -48,6 +48,7 @@ struct Args {
   int M, N, K;
   int mt;   // token rows per tile (multiple of 16, <= MAX_MT)
   int m_tiles;  // token tiles
+  int vec;      // output rows take 16-byte stores (alignment checked on the host)
   int cs;   // CTAs per cluster splitting K (1, 2, 4 or 8)
   int nst;  // ring stages
   int epi;  // Epilogue (launch.h)
@@ -65,7 +66,7 @@ struct Args {
 
 __device__ __forceinline__ uint32_t stage_bytes(int mt) { return W_CHUNK + (uint32_t)mt * 128u; }
 
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, 1)
     wgemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                  const Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -172,11 +173,18 @@ __global__ void __launch_bounds__(THREADS)
   tc_fence_after();
   if (cs == 1) {
     // The whole K range is in this CTA's accumulator: thread r (TMEM lane r)
-    // holds output feature n0 + r for every token of the tile, so it reads
-    // 16 tokens at a time from TMEM and, token by token, the warp writes 32
-    // consecutive features (one contiguous piece of the output row).
+    // holds output feature n0 + r for every token of the tile. It reads 16
+    // tokens at a time from TMEM, applies RoPE (the pair partner is the
+    // neighbouring lane) and parks the values in a [tokens][128 features]
+    // tile in the idle ring; then the CTA writes every token's 128 features
+    // as one contiguous run with 16-byte stores. (Without the alignment for
+    // 16-byte stores each warp stores its 32 features of a token directly.)
     const int r = threadIdx.x, gn = n0 + r;
     const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    const int esz = a.out_f32 ? 4 : 2;
+    const int RB = TILE_N * esz;  // bytes of one staged token row
+    uint8_t* stg = smem;          // [mt][TILE_N] values, reuses the ring
+    long long* rowoff = reinterpret_cast<long long*>(smem + (size_t)mt * RB);  // [mt] output row (elements), -1: none
     int rk = -1;  // RoPE pair of this feature (-1: none) and its side
     bool odd = false;
     if (a.epi == EPI_ROPE || a.epi == EPI_APPEND) {
@@ -186,6 +194,25 @@ __global__ void __launch_bounds__(THREADS)
         odd = ((col - a.rope_off) & 1) != 0;
       }
     }
+    // the output row of token r of the tile (one thread per token)
+    long long my_row = -1;
+    if (r < mt && m0 + r < a.M && mma_ok) {
+      const int gm = m0 + r;
+      if (a.epi == EPI_APPEND) {
+        const int sq = a.seq_idx ? a.seq_idx[gm] : gm;
+        const int ps = a.pos[gm];
+        if (sq < 0 || sq >= a.B || ps < 0 || ps >= a.max_pages * a.page_size) {
+          report(a.dev_status, MLA_DEV_BAD_POS);
+        } else {
+          const int blk = a.block_table[(size_t)sq * a.max_pages + ps / a.page_size];
+          if (blk < 0 || blk >= a.num_pages) report(a.dev_status, MLA_DEV_BAD_BLOCK);
+          else my_row = ((long long)blk * a.page_size + ps % a.page_size) * (long long)a.N;
+        }
+      } else {
+        my_row = (long long)gm * a.ldo;
+      }
+    }
+    if (a.vec && r < mt) rowoff[r] = my_row;
     for (int j0 = 0; j0 < mt; j0 += 16) {
       uint32_t v[16];
       if (mma_ok) {
@@ -197,7 +224,7 @@ __global__ void __launch_bounds__(THREADS)
       }
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        const int gm = m0 + j0 + u;
+        const int j = j0 + u, gm = m0 + j;
         float x = __uint_as_float(v[u]);
         const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
         if (gm >= a.M || !mma_ok) continue;
@@ -210,26 +237,38 @@ __global__ void __launch_bounds__(THREADS)
             x = odd ? partner * cs2.y + x * cs2.x : x * cs2.x - partner * cs2.y;
           }
         }
-        size_t o;
+        if (a.vec) {
+          if (a.out_f32) reinterpret_cast<float*>(stg + (size_t)j * RB)[r] = x;
+          else reinterpret_cast<__nv_bfloat16*>(stg + (size_t)j * RB)[r] = __float2bfloat16_rn(x);
+          continue;
+        }
+        if (gn >= a.N) continue;
+        long long o;
         if (a.epi == EPI_APPEND) {
           const int sq = a.seq_idx ? a.seq_idx[gm] : gm;
           const int ps = a.pos[gm];
-          if (sq < 0 || sq >= a.B || ps < 0 || ps >= a.max_pages * a.page_size) {
-            report(a.dev_status, MLA_DEV_BAD_POS);
-            continue;
-          }
+          if (sq < 0 || sq >= a.B || ps < 0 || ps >= a.max_pages * a.page_size) continue;
           const int blk = a.block_table[(size_t)sq * a.max_pages + ps / a.page_size];
-          if (blk < 0 || blk >= a.num_pages) {
-            report(a.dev_status, MLA_DEV_BAD_BLOCK);
-            continue;
-          }
-          o = ((size_t)blk * a.page_size + ps % a.page_size) * (size_t)a.N + gn;
+          if (blk < 0 || blk >= a.num_pages) continue;
+          o = ((long long)blk * a.page_size + ps % a.page_size) * (long long)a.N + gn;
         } else {
-          o = (size_t)gm * (size_t)a.ldo + gn;
+          o = (long long)gm * a.ldo + gn;
         }
-        if (gn >= a.N) continue;
         if (a.out_f32) reinterpret_cast<float*>(a.out)[o] = x;
         else reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16_rn(x);
+      }
+    }
+    if (a.vec) {
+      __syncthreads();
+      const int per16 = 16 / esz;        // elements per 16-byte piece
+      const int cpr = RB / 16;           // pieces per token row
+      for (int c = r; c < mt * cpr; c += THREADS) {
+        const int j = c / cpr, q = c % cpr;
+        const long long row = rowoff[j];
+        const int g0 = n0 + q * per16;
+        if (row < 0 || g0 >= a.N) continue;
+        const uint4 val = *reinterpret_cast<const uint4*>(stg + (size_t)j * RB + (size_t)q * 16);
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.out) + (size_t)(row + g0) * esz) = val;
       }
     }
     __syncthreads();
@@ -389,6 +428,14 @@ cudaError_t tc_gemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s) {
   a.pos = g.pos; a.seq_idx = g.seq_idx; a.block_table = g.block_table; a.B = g.B;
   a.max_pages = g.max_pages; a.num_pages = g.num_pages; a.page_size = g.page_size;
   a.dev_status = g.dev_status;
+  {
+    // 16-byte output stores need every 8 (bf16) or 4 (fp32) features of a
+    // row in one aligned piece: an aligned base, the row stride and N in
+    // whole pieces
+    const long long per16 = g.o_f32 ? 4 : 8;
+    const long long stride = g.epi == EPI_APPEND ? (long long)N : a.ldo;
+    a.vec = (reinterpret_cast<uintptr_t>(g.out) % 16 == 0) && stride % per16 == 0 && N % per16 == 0;
+  }
   if (g.epi != EPI_STORE && (g.rope_off % 2 != 0)) return cudaErrorInvalidValue;
 
   CUtensorMap tm_w, tm_x;
