@@ -93,6 +93,12 @@ int pick_path(mla_dtype dt, const mla_dims* d) {
   return g_forced_path == 2 ? 2 : 1;
 }
 
+int plan_unit(int path, int rows, int max_pages, int page_size, int workers) {
+  if (path == 0 && page_size > 32 && page_size % 32 == 0 && (long long)rows * max_pages < workers)
+    return 32;
+  return page_size;
+}
+
 int workers_for(int path) {
   const int sms = device_sms();
   if (sms <= 0) return 0;
@@ -115,7 +121,7 @@ cudaError_t launch_decode(const DecodeSetup& ds, const void* q_cat, const void* 
                            softmax_scale, ws, ds.L, o_lat, lse, dev_status, ds.q_len, s);
   return launch_simt_decode(q_cat, cache, block_table, max_pages, num_pages, rows, ds.workers,
                             softmax_scale, ws, ds.L, o_lat, lse, d->n_h, d->d_c, d->d_r,
-                            d->page_size, dtype == MLA_F32 ? 1 : (dtype == MLA_FP8_E4M3 ? 2 : 0),
+                            d->page_size, ds.unit, dtype == MLA_F32 ? 1 : (dtype == MLA_FP8_E4M3 ? 2 : 0),
                             dev_status, ds.q_len, s);
 }
 
@@ -132,6 +138,7 @@ mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* blo
   out->path = 0;
   out->workers = 0;
   out->q_len = q_len;
+  out->unit = dims->page_size;
   if (B == 0) return MLA_OK;
   REQUIRE(q_cat && cache && block_table && seq_lens && o_lat && lse, "NULL tensor argument");
   REQUIRE(max_pages > 0 && num_pages > 0, "max_pages and num_pages must be > 0");
@@ -139,6 +146,7 @@ mla_status decode_setup(const void* q_cat, const void* cache, const int32_t* blo
   out->path = pick_path(dtype, dims);
   out->workers = workers_for(out->path);
   if (out->workers <= 0) return fail(MLA_ERR_CUDA, "cannot query the device's SM count");
+  out->unit = plan_unit(out->path, B * q_len, max_pages, dims->page_size, out->workers);
   out->L = workspace_layout(B * q_len, out->workers, dims->n_h, dims->d_c);
   return MLA_OK;
 }
@@ -469,7 +477,8 @@ mla_status mla_plan_decode_mtp(const int32_t* seq_lens, int B, int q_len, int ma
   const WorkspaceLayout L = workspace_layout(B * q_len, workers, dims->n_h, dims->d_c);
   if (!workspace || ws_bytes < L.total)
     return fail(MLA_ERR_WORKSPACE, "workspace %zu bytes < %zu required", ws_bytes, L.total);
-  return cuda_status(launch_plan(seq_lens, B, q_len, max_pages, dims->page_size, workers, path,
+  const int unit = plan_unit(path, B * q_len, max_pages, dims->page_size, workers);
+  return cuda_status(launch_plan(seq_lens, B, q_len, max_pages * (dims->page_size / unit), unit, workers, path,
                                  dtype != MLA_F32, workspace, L, dev_status, S(stream)),
                      "plan_decode");
 }

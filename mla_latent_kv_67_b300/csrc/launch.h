@@ -60,7 +60,7 @@ cudaError_t launch_to_bf16(const float* src, void* dst, long long n, cudaStream_
 cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32_t* block_table,
                                int max_pages, int num_pages, int B, int workers, float scale,
                                const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
-                               int n_h, int d_c, int d_r, int page_size, int f32,
+                               int n_h, int d_c, int d_r, int page_size, int unit, int f32,
                                int32_t* dev_status, int bt_div, cudaStream_t s);
 // (f32: 1 = fp32 cache and queries, 0 = bf16, 2 = the FP8 row format with
 // bf16 queries.)
@@ -86,8 +86,14 @@ int workers_for(int path);                       // workers the plan cuts the pa
 struct DecodeSetup {
   int path, workers;
   int q_len;        // new tokens per sequence (query rows = B * q_len)
+  int unit;         // tokens per plan unit (plan_unit)
   WorkspaceLayout L;
 };
+// Tokens per unit of the split plan: the page, except on the CUDA-core path
+// when the batch's pages cannot give every worker one (then 32 tokens, the
+// kernel's token tile, so a short batch still spreads over the SMs). The
+// plan and the decode call derive it from the same arguments.
+int plan_unit(int path, int rows, int max_pages, int page_size, int workers);
 // Validates the arguments of a decode call exactly as mla_decode_attn does
 // and picks its kernel, worker count and workspace layout. B == 0 is valid
 // (nothing to do; `out` then has workers == 0).

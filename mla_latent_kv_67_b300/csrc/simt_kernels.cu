@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(256) simt_decode_kernel(
     const T* __restrict__ q_cat, const Rows cache, const int32_t* __restrict__ block_table,
     int max_pages, int num_pages, int B, float scale, const char* __restrict__ ws, WorkspaceLayout L,
     float* __restrict__ o_lat, float* __restrict__ lse_out, int n_h, int d_c, int d_r,
-    int page_size, int32_t* dev_status, int bt_div) {
+    int page_size, int unit, int32_t* dev_status, int bt_div) {
   extern __shared__ float smem[];
   const int W = d_c + d_r, Wp = W + 1;
   float* tile = smem;                     // [SD_TOK][Wp]
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(256) simt_decode_kernel(
     const int p0 = s == wp.seq_begin ? wp.page_begin : 0;
     const int p1 = s == wp.seq_end ? wp.page_end + 1 : sp.pages;
     if (p0 >= p1) continue;
-    const int tok0 = p0 * page_size, tok1 = min(p1 * page_size, sp.len);
+    const int tok0 = p0 * unit, tok1 = min(p1 * unit, sp.len);  // plan units of `unit` tokens
 
     __syncthreads();
     for (int i = threadIdx.x; i < SD_HEADS * W; i += blockDim.x) {
@@ -372,7 +372,7 @@ static cudaError_t simt_decode_launch(const T* q_cat, const Rows& rows, const in
                                       int max_pages, int num_pages, int B, int workers, float scale,
                                       const void* ws, const WorkspaceLayout& L, float* o_lat,
                                       float* lse, int n_h, int d_c, int d_r, int page_size,
-                                      int32_t* dev_status, int bt_div, cudaStream_t s) {
+                                      int unit, int32_t* dev_status, int bt_div, cudaStream_t s) {
   const int W = d_c + d_r;
   const size_t smem = sizeof(float) * ((size_t)SD_TOK * (W + 1) + (size_t)SD_HEADS * W);
   const dim3 grid(workers, (n_h + SD_HEADS - 1) / SD_HEADS);
@@ -381,7 +381,7 @@ static cudaError_t simt_decode_launch(const T* q_cat, const Rows& rows, const in
   if (e != cudaSuccess) return e;
   simt_decode_kernel<T, Rows><<<grid, 256, smem, s>>>(q_cat, rows, block_table, max_pages,
                                                       num_pages, B, scale, (const char*)ws, L,
-                                                      o_lat, lse, n_h, d_c, d_r, page_size,
+                                                      o_lat, lse, n_h, d_c, d_r, page_size, unit,
                                                       dev_status, bt_div);
   return cudaGetLastError();
 }
@@ -389,23 +389,23 @@ static cudaError_t simt_decode_launch(const T* q_cat, const Rows& rows, const in
 cudaError_t launch_simt_decode(const void* q_cat, const void* cache, const int32_t* block_table,
                                int max_pages, int num_pages, int B, int workers, float scale,
                                const void* ws, const WorkspaceLayout& L, float* o_lat, float* lse,
-                               int n_h, int d_c, int d_r, int page_size, int f32,
+                               int n_h, int d_c, int d_r, int page_size, int unit, int f32,
                                int32_t* dev_status, int bt_div, cudaStream_t s) {
   if (B == 0) return cudaSuccess;
   const int W = d_c + d_r;
   if (f32 == 1)
     return simt_decode_launch((const float*)q_cat, ElemRows<float>{(const float*)cache, W},
                               block_table, max_pages, num_pages, B, workers, scale, ws, L, o_lat,
-                              lse, n_h, d_c, d_r, page_size, dev_status, bt_div, s);
+                              lse, n_h, d_c, d_r, page_size, unit, dev_status, bt_div, s);
   if (f32 == 0)
     return simt_decode_launch((const __nv_bfloat16*)q_cat,
                               ElemRows<__nv_bfloat16>{(const __nv_bfloat16*)cache, W}, block_table,
                               max_pages, num_pages, B, workers, scale, ws, L, o_lat, lse, n_h, d_c,
-                              d_r, page_size, dev_status, bt_div, s);
+                              d_r, page_size, unit, dev_status, bt_div, s);
   // FP8 latent cache, bf16 queries
   const Fp8Rows rows{(const uint8_t*)cache, MLA_FP8_ROW_BYTES(d_c, d_r), d_c, d_r};
   return simt_decode_launch((const __nv_bfloat16*)q_cat, rows, block_table, max_pages, num_pages,
-                            B, workers, scale, ws, L, o_lat, lse, n_h, d_c, d_r, page_size,
+                            B, workers, scale, ws, L, o_lat, lse, n_h, d_c, d_r, page_size, unit,
                             dev_status, bt_div, s);
 }
 

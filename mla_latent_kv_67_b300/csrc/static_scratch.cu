@@ -82,7 +82,8 @@ extern "C" mla_status mla_decode_attn_static(const void* q_cat, const void* cach
   // Nothing in the scratch needs to start at zero: the plan kernel rewrites
   // every plan entry it reads back, and each partial slot is written by the
   // decode kernel before the combine kernel reads it.
-  e = launch_plan(seq_lens, B, 1, max_pages, d->page_size, ds.workers, ds.path, dtype != MLA_F32,
+  e = launch_plan(seq_lens, B, 1, max_pages * (d->page_size / ds.unit), ds.unit, ds.workers, ds.path,
+                  dtype != MLA_F32,
                   ws, ds.L, dev_status, s);
   if (e == cudaSuccess)
     e = launch_decode(ds, q_cat, cache, block_table, max_pages, num_pages, B, softmax_scale, ws,
