@@ -351,14 +351,16 @@ def capture(fn):
     return g
 
 
-def measure_workload(wl, dev, K, W, flush, stream, hbm, tflops, barrier=None, sampler=None):
+def measure_workload(wl, dev, K, W, flush, stream, hbm, tflops, barrier=None, sampler=None,
+                     fp8_staged=False):
     """Step and per-stage times of one workload: the step as one CUDA graph
     (value), each stage as a graph of its own timed alone, the decode
-    kernel's roofline."""
+    kernel's roofline. fp8_staged: the FP8 cache through the widening entry
+    point (its attention stage then holds widen, plan, decode and merge)."""
     import torch
     from mla_latent_kv_67_b300 import binding as M
     from mla_latent_kv_67_b300.step import DecodeStep
-    st = DecodeStep(wl, device=dev)
+    st = DecodeStep(wl, device=dev, fp8_staged=fp8_staged)
     for _ in range(W):
         flush()
         st.run()
@@ -387,7 +389,8 @@ def measure_workload(wl, dev, K, W, flush, stream, hbm, tflops, barrier=None, sa
     torch.cuda.synchronize()
     assert st.status() == 0, f"{wl.name}: device status {st.status():#x}"
     prefill = wl.mode == "prefill_mha"
-    kernel_us = stages["prefill" if prefill else "attend"]
+    kernel_us = stages["prefill" if prefill else
+                       ("attend_fp8_staged" if fp8_staged else "attend")]
     alg_bytes, alg_flops = algorithmic_prefill(wl) if prefill else algorithmic(wl, st.lens_np)
     t_hbm = alg_bytes / (hbm * 1e9)
     t_flop = alg_flops / (tflops * 1e12)
@@ -401,13 +404,17 @@ def measure_workload(wl, dev, K, W, flush, stream, hbm, tflops, barrier=None, sa
             "unit": "TFLOP/s" if tensor_bound else "GB/s",
             "frac": tensor / tflops if tensor_bound else achieved / hbm,
             "traffic": DECODE_TRAFFIC.get(wl.name) if path == 1 else None,
-            "kernel": "mla_prefill_attn" if prefill else "mla_decode_attn", "kernel_us": kernel_us,
+            "kernel": "mla_prefill_attn" if prefill else
+                      ("mla_decode_attn_fp8_staged" if fp8_staged else "mla_decode_attn"),
+            "kernel_us": kernel_us,
             "alg_bytes": alg_bytes, "alg_flops": alg_flops,
             "tensor_tflops": tensor, "tensor_peak": tflops, "tensor_frac": tensor / tflops,
             "roofline_us": max(t_hbm, t_flop) * 1e6,
             "frac_of_roofline": max(t_hbm, t_flop) * 1e6 / kernel_us}
     return st, g, {"step_us": step_ms * 1e3, "stages_us": stages, "roofline": roof,
-                   "decode_kernel": DECODE_KERNELS.get(path, "simt"),
+                   "decode_kernel": (DECODE_KERNELS.get(M.mla_decode_path(M.MLA_BF16, st.dims))
+                                     + " on bf16-widened pages") if fp8_staged else
+                                    DECODE_KERNELS.get(path, "simt"),
                    "step_roofline": None if prefill else
                    step_roofline(wl, st.lens_np, hbm, tflops, step_ms * 1e3)}
 
@@ -585,9 +592,11 @@ def main():
         for name in OTHER_WORKLOADS:
             if name == wl.name:
                 continue
-            ow = synth.WORKLOADS.get(name) or synth.EXTRA_WORKLOADS[name]
+            staged = name.endswith(STAGED)
+            base = name[:-len(STAGED)] if staged else name
+            ow = synth.WORKLOADS.get(base) or synth.EXTRA_WORKLOADS[base]
             ost, og, ores = measure_workload(ow, dev, max(3, min(K, 20)), max(3, min(args.warmup, 5)),
-                                             flush, stream, hbm, tflops)
+                                             flush, stream, hbm, tflops, fp8_staged=staged)
             ores["roofline"]["peak_source"] = peak_kind
             ores["config"] = {"batch": ow.batch, "ctx_total": int(ost.lens_np.sum()),
                               "ctx_max": int(ost.lens_np.max()), "mode": ow.mode,
@@ -609,7 +618,10 @@ def main():
 # workload is a parity case only)
 OTHER_WORKLOADS = ("dsv2_b4_ctx128k", "dsv2_b128_ragged", "dsv2_layer_b64_ctx32k",
                    "dsv2_layer_b64_ctx32k_fused", "dsv2_b32_ctx4k_mtp2", "dsv2_prefill_4k",
-                   "dsv2_b32_ctx4k_fp8")
+                   "dsv2_b32_ctx4k_fp8", "dsv2_b32_ctx4k_fp8_staged")
+# an entry named <workload> + STAGED: that FP8 workload through
+# mla_decode_attn_fp8_staged instead of the CUDA-core FP8 kernel
+STAGED = "_staged"
 
 
 if __name__ == "__main__":

@@ -335,6 +335,35 @@ mla_status mla_decode_attn_static(const void* q_cat, const void* cache,
                                   float* o_lat, float* lse, mla_dtype dtype,
                                   const mla_dims* dims, int32_t* dev_status, void* stream);
 
+/* Decode on the FP8 latent cache through the bf16 decode kernels
+ * (DeepSeek-V2 MLA page 5.1 item 3: the absorbed path kept on a quantized
+ * cache). The call widens every page the batch reads into bf16 rows
+ * (c_KV[i] = bf16(e4m3(code[i]) * s), k_R copied) in the workspace, under an
+ * identity block table, then plans, decodes and combines those rows exactly
+ * as mla_decode_attn with dtype MLA_BF16 does (the tcgen05 kernel wherever
+ * it supports the shape). o_lat and lse are final; no mla_combine follows.
+ *   q_cat      [B][n_h][d_c + d_r] bf16, device.
+ *   cache      [num_pages][page_size][MLA_FP8_ROW_BYTES(d_c, d_r)] bytes in
+ *              the FP8 row format above, device, 16-byte aligned.
+ *   block_table, max_pages, num_pages, seq_lens, B, softmax_scale, o_lat,
+ *              lse, dev_status, stream: as mla_decode_attn.
+ *   workspace  >= mla_decode_fp8_staged_workspace_size(B, max_pages, dims)
+ *              bytes of device memory, 256-byte aligned, owned by the
+ *              caller; nothing in it has to start at zero. It holds the
+ *              bf16 plan and partials, the identity table and
+ *              B * max_pages * page_size * (d_c + d_r) bf16 rows.
+ * Errors: as mla_decode_attn; MLA_ERR_UNSUPPORTED for B > 65535 or d_r not
+ * a multiple of 8. Block ids outside [0, num_pages) are reported through
+ * dev_status (MLA_DEV_BAD_BLOCK) and read as zero rows. The workspace size
+ * depends on the decode kernel the device selects; query it under the same
+ * mla_force_decode_path setting as the call. */
+size_t mla_decode_fp8_staged_workspace_size(int B, int max_pages, const mla_dims* dims);
+mla_status mla_decode_attn_fp8_staged(const void* q_cat, const void* cache,
+                                      const int32_t* block_table, int max_pages, int num_pages,
+                                      const int32_t* seq_lens, int B, float softmax_scale,
+                                      void* workspace, size_t ws_bytes, float* o_lat, float* lse,
+                                      const mla_dims* dims, int32_t* dev_status, void* stream);
+
 /* Diagnostic for the tensor-core decode kernel's data path (no counterpart
  * in the method): one 64-token page through the same tcgen05 operand
  * layouts, without softmax. All bf16 row-major device tensors:

@@ -60,6 +60,9 @@ _SIGS = {
                                  _P]),
     "mla_combine": (_I, [_P, _S, _I, _P, _P, _I, _DIMS, _P]),
     "mla_decode_attn_static": (_I, [_P, _P, _P, _I, _I, _P, _I, _F, _P, _P, _I, _DIMS, _P, _P]),
+    "mla_decode_fp8_staged_workspace_size": (_S, [_I, _I, _DIMS]),
+    "mla_decode_attn_fp8_staged": (_I, [_P, _P, _P, _I, _I, _P, _I, _F, _P, _S, _P, _P, _DIMS, _P,
+                                        _P]),
     "mla_absorb_out": (_I, [_P, _P, _P, _I, _I, _I, _DIMS, _P]),
     "mla_combine_absorb_out": (_I, [_P, _S, _I, _P, _P, _P, _P, _I, _I, _DIMS, _P, _P]),
     "mla_tc_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
@@ -321,6 +324,28 @@ def mla_decode_attn_static(q_cat, cache, block_table, seq_lens, scale: float, o_
         _ptr(seq_lens, torch.int32, (B,), "seq_lens"), B, scale,
         _ptr(o_lat, torch.float32, (B, dims.n_h, dims.d_c), "o_lat"),
         _ptr(lse, torch.float32, (B, dims.n_h), "lse"), dt, ctypes.byref(dims),
+        _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
+
+
+def mla_decode_fp8_staged_workspace_size(B: int, max_pages: int, dims: Dims) -> int:
+    return int(lib().mla_decode_fp8_staged_workspace_size(B, max_pages, ctypes.byref(dims)))
+
+
+def mla_decode_attn_fp8_staged(q_cat, cache, block_table, seq_lens, scale: float, workspace,
+                               o_lat, lse, dims: Dims, dev_status=None, stream=None) -> None:
+    """Decode on the FP8 latent cache by widening the batch's pages to bf16
+    rows in `workspace` and running the bf16 decode on them (see the header)."""
+    B, max_pages = block_table.shape
+    if cache.dtype != torch.uint8:
+        raise MlaError(MLA_ERR_INVALID_ARG, "cache must be the FP8 row format (uint8)")
+    _check(lib().mla_decode_attn_fp8_staged(
+        _ptr(q_cat, torch.bfloat16, (B, dims.n_h, dims.d_c + dims.d_r), "q_cat"),
+        _ptr(cache, shape=_cache_shape(cache, dims), name="cache"),
+        _ptr(block_table, torch.int32, name="block_table"), max_pages, cache.shape[0],
+        _ptr(seq_lens, torch.int32, (B,), "seq_lens"), B, scale,
+        _ptr(workspace, torch.uint8, name="workspace"), workspace.numel(),
+        _ptr(o_lat, torch.float32, (B, dims.n_h, dims.d_c), "o_lat"),
+        _ptr(lse, torch.float32, (B, dims.n_h), "lse"), ctypes.byref(dims),
         _ptr(dev_status, torch.int32, name="dev_status"), _stream(stream)))
 
 

@@ -33,8 +33,13 @@ def to_device(arr: np.ndarray, wl: synth.Workload, device) -> torch.Tensor:
 
 
 class DecodeStep:
-    def __init__(self, wl: synth.Workload, device="cuda", out_dtype=None):
+    def __init__(self, wl: synth.Workload, device="cuda", out_dtype=None, fp8_staged=False):
+        """fp8_staged: on the FP8 cache (one new token per sequence), decode
+        with mla_decode_attn_fp8_staged (pages widened to bf16, then the bf16
+        decode kernels) instead of the CUDA-core FP8 kernel."""
         self.wl, self.device = wl, torch.device(device)
+        assert not fp8_staged or (wl.dtype == "fp8" and wl.q_len == 1)
+        self.fp8_staged = fp8_staged
         self.dims = M.Dims.of(wl)
         self.dtype = {"bf16": M.MLA_BF16, "f32": M.MLA_F32, "fp8": M.MLA_FP8_E4M3}[wl.dtype]
         tdt = M.torch_dtype(self.dtype)
@@ -100,7 +105,8 @@ class DecodeStep:
             self.lse_pf = torch.empty((N, n_h), dtype=torch.float32, device=dev)
         R = B * wl.q_len  # query rows
         self.q_cat = torch.empty((R, n_h, wl.d_c + wl.d_r), dtype=tdt, device=dev)
-        ws = M.mla_decode_workspace_size(R, self.dtype, self.dims)
+        ws = (M.mla_decode_fp8_staged_workspace_size(R, bt.shape[1], self.dims) if fp8_staged
+              else M.mla_decode_workspace_size(R, self.dtype, self.dims))
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev)
         self.o_lat = torch.empty((R, n_h, wl.d_c), dtype=torch.float32, device=dev)
         self.lse = torch.empty((R, n_h), dtype=torch.float32, device=dev)
@@ -147,6 +153,11 @@ class DecodeStep:
                               self.wl.scale, self.workspace, self.o_lat, self.lse, self.dims,
                               self.dev_status)
 
+    def attend_fp8_staged(self):
+        M.mla_decode_attn_fp8_staged(self.q_cat, self.cache, self.block_table, self.seq_lens,
+                                     self.wl.scale, self.workspace, self.o_lat, self.lse,
+                                     self.dims, self.dev_status)
+
     def combine(self):
         M.mla_combine(self.workspace, self.o_lat, self.lse, self.dtype, self.dims)
 
@@ -180,6 +191,8 @@ class DecodeStep:
     def stages(self):
         if self.wl.mode == "prefill_mha":
             return [self.append, self.project, self.gather, self.expand, self.prefill]
+        if self.fp8_staged:  # plan and merge inside the call
+            return [self.absorb_q, self.attend_fp8_staged, self.absorb_out]
         if self.wl.fused:
             return [self.append, self.project_absorbed, self.plan, self.attend, self.combine,
                     self.out_absorbed]
@@ -199,7 +212,7 @@ class DecodeStep:
         """One step. The split plan depends only on the lengths, so it runs on
         a side stream next to the stages before attention (both streams
         join before the decode kernel; this also captures into a graph)."""
-        if self.wl.mode == "prefill_mha":
+        if self.wl.mode == "prefill_mha" or self.fp8_staged:
             for f in self.stages():
                 f()
             return
