@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(AM_THREADS, 1)
       n[k] = valid[k] ? sp.n_splits : 0;
       sbeg[k] = sp.slot_begin;
     }
-    // round 0 of both rows: a split past the end re-reads the last one
+    // first batch of splits of both rows: a split past the end re-reads the last one
     // (weight 0); an unsplit row reads its o_lat row (weight 1)
     float4 x[2][RS][4];
     // float4 column lane + 32 q of split sidx of row k (partials in bf16 or
