@@ -15,10 +15,9 @@
 //
 //   rank 0, the score CTA: Q_cat in TMEM as the A operand, S into TMEM
 //     (three buffers), pages from a 3-stage ring; three MMA issuer threads
-//     take pages in turn (page i into S buffer i % 3). A page's 36 products
-//     all accumulate into one S buffer, so each waits for the one before:
-//     one such chain keeps the tensor core about a third busy at N = 64, and
-//     three chains in flight are needed to fill it. Two groups of four
+//     take pages in turn (page i into S buffer i % 3). One thread issues
+//     N = 64 products at about half the tensor core's rate; two or three
+//     issuing threads together nearly saturate it. Two groups of four
 //     softmax warps take the pages in turn (thread = head row = TMEM lane;
 //     the groups share each page's reference maximum through shared
 //     memory) and turn S into bf16 probabilities P and
@@ -45,8 +44,7 @@
 // Each CTA loads its pages on its own: the second read of a page hits L2 and
 // costs no HBM bandwidth, and neither ring waits for the other. The MMA
 // issuers synchronise once per page (one barrier wait, one fence, one commit
-// per stage), since every such round trip costs about as much as several
-// MMAs.
+// per stage).
 //
 // Online softmax: running maximum in log2 units; O is rescaled only when a
 // row's maximum grows by more than 8 (a factor 256). Until then P is taken
