@@ -40,14 +40,17 @@ cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// A projection: the tcgen05 weight-streaming GEMM for bf16 operands of a
-// shape it takes, the CUDA-core GEMM otherwise (fp32, odd K, or the SIMT
-// path forced for cross-checks).
+// A projection: for bf16 operands of a shape they take, the tcgen05 tile
+// GEMM when there are many tokens (the product is then tensor-core bound)
+// and the weight-streaming GEMM otherwise (few tokens: bound by reading the
+// weights); the CUDA-core GEMM for the rest (fp32, odd K, or the SIMT path
+// forced for cross-checks).
 cudaError_t projection(const GemmArgs& g, cudaStream_t s) {
   if (!g.a_f32 && !g.w_f32 && g.G == 1 && g.w_ks == 1 && g_forced_path != 0 &&
       aligned16(g.a) && aligned16(g.w) && g.w_ns % 8 == 0 &&
       tc_gemm_supported(g.M, g.N, g.K, g.a_ms))
-    return tc_gemm_launch(g, g.a_ms, s);
+    return tc_tgemm_wanted(g.M, g.N, g.K) ? tc_tgemm_launch(g, g.a_ms, s)
+                                           : tc_gemm_launch(g, g.a_ms, s);
   return launch_simt_gemm(g, s);
 }
 

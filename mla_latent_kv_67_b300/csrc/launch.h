@@ -38,6 +38,11 @@ cudaError_t launch_simt_gemm(const GemmArgs& g, cudaStream_t s);
 // stride in elements.
 bool tc_gemm_supported(int M, int N, int K, long long ldx);
 cudaError_t tc_gemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s);
+// tcgen05 tile GEMM for many tokens (tc_tgemm.cu): the same products and
+// epilogues, tiles of 128 tokens x 256 features, tensor-core bound. Taken
+// where tc_tgemm_wanted holds and tc_gemm_supported does.
+bool tc_tgemm_wanted(int M, int N, int K);
+cudaError_t tc_tgemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s);
 cudaError_t launch_copy_rope_part(const void* q, void* q_cat, int B, int n_h, int d_h, int d_r,
                                   int d_c, int f32, cudaStream_t s);
 cudaError_t launch_rope_table(float* cs, int max_pos, int d_r, double base, cudaStream_t s);

@@ -1,5 +1,6 @@
-"""The tcgen05 weight-streaming GEMM behind mla_append_latent, mla_project_q
-and mla_out_proj, through the C ABI.
+"""The tcgen05 GEMMs behind mla_append_latent, mla_project_q, mla_expand_kv
+and mla_out_proj, through the C ABI: the weight-streaming GEMM for few
+tokens and the tile GEMM for 256 tokens or more.
 
 Each product is checked against a float64 product of the same bf16 values
 (fp32 accumulation on the GPU: max |gpu - ref| / max |ref| <= 1e-5 before
@@ -34,6 +35,10 @@ OUT_PROJ_SHAPES = [
     (257, 1, 64, 96),       # three token tiles, K = 64
     (600, 4, 128, 384),     # five token tiles, ragged last, K = 512
     (512, 8, 64, 256),      # four full token tiles x two weight tiles
+    # tile GEMM (>= 256 tokens): 128-token x 256-feature tiles
+    (1024, 16, 128, 768),   # 8 x 3 tiles, K = 2048
+    (2048, 8, 64, 4096),    # 256 tiles: each SM takes two, both accumulators in turn
+    (383, 3, 64, 520),      # ragged last token and feature tiles, K = 192
 ]
 
 
@@ -81,6 +86,28 @@ def test_project_q_epilogue_against_oracle():
                                    wl.n_h, w_dq=None, base=wl.rope_base)
         ref = np.concatenate([q_c, q_r], axis=-1)
         assert np.all(np.abs(q[b] - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max()), b
+
+
+def test_project_q_many_tokens_tile_gemm():
+    """A 300-token prompt's query projection (tile GEMM, RoPE epilogue on the
+    q_R slice of every head): c_Q against x W^DQ^T, q against the oracle's
+    query projection of the GPU's own c_Q, every token."""
+    wl = synth.EXTRA_WORKLOADS["dsv2_prefill_4k"].replace(name="proj_300", ctx=300, seed=62)
+    st = DecodeStep(wl)
+    st.project()
+    torch.cuda.synchronize()
+    assert st.status() == 0
+    x = synth.tokens(wl).astype(np.float64)
+    w_dq = synth.weight(wl, "w_dq").astype(np.float64)
+    cq = st.c_q.double().cpu().numpy()
+    cq_ref = x @ w_dq.T
+    assert np.all(np.abs(cq - cq_ref) <= 2.0 ** -8 * np.abs(cq_ref) + 1e-5 * np.abs(cq_ref).max())
+    q_c, q_r = O.project_query(cq, synth.weight(wl, "w_uq").astype(np.float64),
+                               synth.weight(wl, "w_qr").astype(np.float64), np.arange(wl.ctx),
+                               wl.n_h, w_dq=None, base=wl.rope_base)
+    ref = np.concatenate([q_c, q_r], axis=-1)
+    q = st.q.double().cpu().numpy()
+    assert np.all(np.abs(q - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max())
 
 
 def test_append_many_tokens_across_token_tiles():
