@@ -14,10 +14,11 @@
 // products therefore run on the two CTAs (two SMs) of a cluster, each once:
 //
 //   rank 0, the score CTA: Q_cat in TMEM as the A operand, S into TMEM
-//     (three buffers), pages from a 3-stage ring; three MMA issuer threads
-//     take pages in turn (page i into S buffer i % 3). One thread issues
-//     N = 64 products at about half the tensor core's rate; two or three
-//     issuing threads together nearly saturate it. Two groups of four
+//     (two buffers), pages from a 3-stage ring; two MMA issuer threads
+//     take pages in turn (page i into S buffer i % 2). One thread issues
+//     N = 64 products at about half the tensor core's rate; two issuing
+//     threads together nearly saturate it, and a third only lengthens every
+//     page's product chain (and so how long it holds its ring stage). Two groups of four
 //     softmax warps take the pages in turn (thread = head row = TMEM lane;
 //     the groups share each page's reference maximum through shared
 //     memory) and turn S into bf16 probabilities P and
@@ -73,8 +74,8 @@ constexpr uint32_t CHUNK = PAGE * 128;  // one chunk of a page: 64 tokens x 128 
 constexpr int NKS = 3;                  // score CTA: page stages
 constexpr int NVS = 2;                  // value CTA: latent page stages
 constexpr int NP = 3;                   // P slots
-constexpr int NSB = 3;                  // S buffers in TMEM
-constexpr int NQK = 3;                  // QK issuer threads (page i: issuer and S buffer i % 3)
+constexpr int NSB = 2;                  // S buffers in TMEM
+constexpr int NQK = 2;                  // QK issuer threads (page i: issuer and S buffer i % 2)
 static_assert(NQK == NSB, "each QK issuer owns one S buffer");
 constexpr uint32_t KSTAGE = NCHUNK * CHUNK;
 constexpr int HALF_BLOCKS = DC / 2 / 32;  // 32-column TMEM blocks in one half of O
@@ -106,7 +107,7 @@ enum {
   QEMPTY = QTMEM + 1,    // last QK of a segment done
   PEMPTY = QEMPTY + 1,   // [NP] value CTA done with P slot (its PV commit)
   SFINAL = PEMPTY + NP,  // [NQK] drain after an abort (one per QK issuer)
-  MREADY = SFINAL + 3,   // [2] reference maximum of a page published (4 warps), by page parity
+  MREADY = SFINAL + NQK, // [2] reference maximum of a page published (4 warps), by page parity
   LXREADY = MREADY + 2,  // [2] l of the non-last group published at a sequence's end (4 warps)
   S_NBAR = LXREADY + 2
 };
@@ -144,7 +145,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 static_assert(V_OFF_P % 1024 == 0 && X_BYTES % 16 == 0 && V_OFF_STG % 16 == 0 && V_OFF_BAR % 8 == 0,
               "layout alignment");
 
-// TMEM columns. Score CTA: S0 | S1 | S2 | Q (576 bf16 packed in 288 columns).
+// TMEM columns. Score CTA: S0 | S1 | Q (576 bf16 packed in 288 columns).
 constexpr uint32_t TM_S = 0, TM_Q = 64 * NSB, TM_COLS = 512;
 static_assert(TM_Q + 288 <= TM_COLS, "score CTA TMEM budget");
 
@@ -361,16 +362,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (uint32_t k = rk > (uint32_t)NKS ? rk - NKS : 0; k < rk; ++k)
           mbar_wait_drain(cx.bar(KFULL + k % NKS), (k / NKS) & 1, DRAIN_NS);
       }
-    } else if (warp == 1 || warp == 6 || warp == 7) {
+    } else if (warp == 1 || warp == 6) {
       // --------------------------------------------------------- QK issue
-      // issuer e (warps 1, 6, 7) takes the pages with it % 3 == e, into S
+      // issuer e (warps 1, 6) takes the pages with it % 2 == e, into S
       // buffer e. Each waits for every sequence's Q (so none can fall a
       // phase behind) and arrives once per sequence on QEMPTY: by a commit
       // after its last QK of the sequence, or a plain arrive if it had none
       // (a commit with no new MMA since the thread's previous commit does not
       // arrive).
       if (lane == 0) {
-        const uint32_t e = warp == 1 ? 0u : warp == 6 ? 1u : 2u;
+        const uint32_t e = warp == 1 ? 0u : 1u;  // warp 7 has no role in the score CTA
         uint32_t it = 0, seg = 0;
         bool ok = true;
         for (int s = w.seq_begin; ok && s <= w.seq_end; ++s) {
