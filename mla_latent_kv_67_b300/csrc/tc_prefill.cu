@@ -23,7 +23,9 @@
 // masks keys after the query. Warp 0 streams the key/value tiles with TMA
 // (two stages; a stage's keys are refilled once its S is done, its values
 // once its PV is done, so the next keys do not wait for the PV), warp 1
-// issues the MMAs. Every wait is bounded and reports MLA_DEV_TIMEOUT.
+// issues the S products and warp 6 the P.V products (one issuing thread
+// reaches only about half the tensor core's rate at these shapes; two
+// share it). Every wait is bounded and reports MLA_DEV_TIMEOUT.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -56,8 +58,9 @@ enum {
   SFREE = SFULL + 2,    // [2] (4 warps)
   PFULL = SFREE + 2,    // [2] (4 warps)
   PFREE = PFULL + 2,    // [2] (commit)
-  FIN = PFREE + 2,
-  NBAR = FIN + 1
+  FIN = PFREE + 2,      // drain after an abort: S issuer
+  FIN2 = FIN + 1,       // ... and PV issuer
+  NBAR = FIN2 + 1
 };
 constexpr uint32_t OFF_BAR = OFF_K + NST * KSTAGE;
 constexpr uint32_t OFF_TSLOT = OFF_BAR + 8 * NBAR;
@@ -71,7 +74,7 @@ constexpr uint32_t IDESC_S = idesc_bf16_f32(TQ, TK, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(TQ, DV, false, true);
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 100000000ull;
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;
 
 struct Params {
   int N;                // tokens
@@ -123,6 +126,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar(PFREE + i), 1);
     }
     mbar_init(bar(FIN), 1);
+    mbar_init(bar(FIN2), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -181,25 +185,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait_drain(bar(VFULL + i % NST), (i / NST) & 1, DRAIN_NS);
     mbar_wait_drain(bar(QFULL), 0, DRAIN_NS);
   } else if (warp == 1 && lane == 0) {
-    // ----------------------------------------------------------- MMA issue
-    // S of key tile kt, then PV of tile kt - 1 (so S runs one tile ahead)
+    // ------------------------------------------------------------- S issue
+    // S of key tile kt into S buffer kt & 1; the P.V products come from
+    // warp 6, so the two chains share the tensor pipe instead of taking
+    // turns in one issuing thread
     bool ok = wait1(bar(QFULL), 0, abort_flag, p.dev_status);
     bool any = false;
-    auto pv = [&](int kt) -> bool {
-      const int st = kt % NST, pb = kt & 1;
-      if (!wait1(bar(PFULL + pb), (kt >> 1) & 1, abort_flag, p.dev_status) ||
-          !wait1(bar(VFULL + st), (kt / NST) & 1, abort_flag, p.dev_status))
-        return false;
-      tc_fence_after();
-      const uint32_t vt = sb + OFF_K + st * KSTAGE + NQC * CH;
-#pragma unroll
-      for (int kk = 0; kk < TK / 16; ++kk)
-        mma_ts(tmem + TM_O, tmem + TM_P + pb * 64 + kk * 8, sdesc_sw128(vt + kk * 2048, CH, 1024),
-               IDESC_PV, (kt > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(bar(PFREE + pb));
-      mma_commit(bar(VEMPTY + st));
-      return true;
-    };
     for (int kt = 0; ok && kt < nkt; ++kt) {
       const int st = kt % NST, sbuf = kt & 1;
       ok = wait1(bar(SFREE + sbuf), ((kt >> 1) & 1) ^ 1, abort_flag, p.dev_status) &&
@@ -215,14 +206,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                  sdesc_sw128(kt_base + c * CH + kk * 32, 16, 1024), IDESC_S, (c | kk) ? 1u : 0u);
       mma_commit(bar(SFULL + sbuf));
       any = true;
-      if (kt > 0) ok = pv(kt - 1);
     }
-    if (ok) ok = pv(nkt - 1);
     if (!ok && any) {
       mma_commit(bar(FIN));
       mbar_wait_drain(bar(FIN), 0, DRAIN_NS);
     }
-  } else if (warp >= 2) {
+  } else if (warp == 6 && lane == 0) {
+    // ------------------------------------------------------------ PV issue
+    bool ok = true, any = false;
+    for (int kt = 0; ok && kt < nkt; ++kt) {
+      const int st = kt % NST, pb = kt & 1;
+      ok = wait1(bar(PFULL + pb), (kt >> 1) & 1, abort_flag, p.dev_status) &&
+           wait1(bar(VFULL + st), (kt / NST) & 1, abort_flag, p.dev_status);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t vt = sb + OFF_K + st * KSTAGE + NQC * CH;
+#pragma unroll
+      for (int kk = 0; kk < TK / 16; ++kk)
+        mma_ts(tmem + TM_O, tmem + TM_P + pb * 64 + kk * 8, sdesc_sw128(vt + kk * 2048, CH, 1024),
+               IDESC_PV, (kt > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(bar(PFREE + pb));
+      mma_commit(bar(VEMPTY + st));
+      any = true;
+    }
+    if (!ok && any) {
+      mma_commit(bar(FIN2));
+      mbar_wait_drain(bar(FIN2), 0, DRAIN_NS);
+    }
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------- softmax
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
