@@ -9,10 +9,13 @@
 // With thousands of tokens the product is bound by the tensor cores, not by
 // the weight bytes, so the tile is the token side as the MMA's M (128 token
 // rows) and 256 output features as N: D[128 tokens][256 features] in tensor
-// memory, one 128 x 256 x 16 product per instruction. A persistent CTA per
-// SM walks its tiles (token tiles fastest, so the CTAs in flight share a few
-// weight tiles in L2):
-//   warp 0     TMA producer: X and W chunks of 64 along K into a 4-stage ring;
+// memory, one 128 x 256 x 16 product per instruction. Persistent clusters of
+// two CTAs (one per SM) walk pairs of tiles that share their 256 features
+// (token tiles fastest, so the clusters in flight share a few weight tiles in
+// L2); each CTA of a pair loads half of every weight chunk and multicasts it
+// to both:
+//   warp 0     TMA producer: X and W chunks of 64 along K into a 4-stage ring
+//              (a stage is refilled once the products of both CTAs are done);
 //   warp 1     MMA issuer: four products per chunk into one of two
 //              accumulators (256 columns each), so the epilogue of a tile
 //              overlaps the products of the next;
@@ -48,9 +51,21 @@ constexpr uint32_t IDESC = idesc_bf16_f32(TM, TN, false, false);
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_NS = 100000000ull;
 
+// 2-D tiled load global -> shared, written at the same shared offset in every
+// CTA of `mask` in the cluster, completion counted on `bar` (same offset) in
+// each of them.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
+}
+
 struct Args {
   int M, N, K;
-  int m_tiles, tiles;
+  int m_pairs, tiles;  // tiles: pairs of token tiles x feature tiles
   int vec;  // output rows take 16-byte stores (alignment checked on the host)
   int epi;
   void* out;
@@ -65,7 +80,7 @@ struct Args {
   int32_t* dev_status;
 };
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tgemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                  const Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -77,13 +92,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + OFF_TSLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
   const int nc = a.K / 64;
+  // A cluster of two takes tiles in pairs: the same 256 features for two
+  // token tiles. Each CTA loads half of the weight chunk and multicasts it to
+  // both, so a pair reads each weight chunk from L2 once.
+  const uint32_t rank = cluster_ctarank();
+  const int cl = (int)blockIdx.x >> 1, ncl = (int)gridDim.x >> 1;
+  auto tile_n0 = [&](int t) { return (t / a.m_pairs) * TN; };
+  auto tile_m0 = [&](int t) { return ((t % a.m_pairs) * 2 + (int)rank) * TM; };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_w);
     for (int i = 0; i < NST; ++i) {
       mbar_init(bar(FULL + i), 1);
-      mbar_init(bar(EMPTY + i), 1);
+      mbar_init(bar(EMPTY + i), 2);  // both CTAs' products read the stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(TFULL + i), 1);
@@ -101,35 +123,40 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  cluster_sync_all();  // both CTAs' barriers initialised before any multicast
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t kc = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < a.tiles; t += gridDim.x) {
-        const int n0 = (t / a.m_tiles) * TN, m0 = (t % a.m_tiles) * TM;
+      for (int t = cl; ok && t < a.tiles; t += ncl) {
+        const int n0 = tile_n0(t), m0 = tile_m0(t);
         for (int c = 0; c < nc; ++c, ++kc) {
           const uint32_t st = kc % NST;
           ok = mbar_wait_bounded(bar(EMPTY + st), ((kc / NST) & 1) ^ 1, abort_flag, a.dev_status,
                                  WAIT_NS);
           if (!ok) break;
           const uint32_t dst = sb + st * STAGE;
-          mbar_expect_tx(bar(FULL + st), STAGE);
+          mbar_expect_tx(bar(FULL + st), STAGE);  // own X chunk + both weight halves
           tma_load_2d(dst, &tm_x, 64 * c, m0, bar(FULL + st));
-          tma_load_2d(dst + A_BYTES, &tm_w, 64 * c, n0, bar(FULL + st));
+          tma_load_2d_mc(dst + A_BYTES + rank * (B_BYTES / 2), &tm_w, 64 * c, n0 + (int)rank * (TN / 2),
+                         bar(FULL + st), (uint16_t)3);
         }
       }
-      // copies still in flight land before the CTA may exit
-      for (uint32_t k = kc > (uint32_t)NST ? kc - NST : 0; k < kc; ++k)
+      // copies still in flight land, and the peer's products are done with
+      // every stage (its commits arrive here), before the CTA may exit
+      for (uint32_t k = kc > (uint32_t)NST ? kc - NST : 0; k < kc; ++k) {
         mbar_wait_drain(bar(FULL + k % NST), (k / NST) & 1, DRAIN_NS);
+        mbar_wait_drain(bar(EMPTY + k % NST), (k / NST) & 1, DRAIN_NS);
+      }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issue
     if (lane == 0) {
       uint32_t kc = 0, i = 0;
       bool ok = true, any = false;
-      for (int t = blockIdx.x; ok && t < a.tiles; t += gridDim.x, ++i) {
+      for (int t = cl; ok && t < a.tiles; t += ncl, ++i) {
         const uint32_t acc = i & 1u, d = tmem + acc * TN;
         ok = mbar_wait_bounded(bar(TEMPTY + acc), ((i >> 1) & 1) ^ 1, abort_flag, a.dev_status,
                                WAIT_NS);
@@ -145,7 +172,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int kk = 0; kk < 4; ++kk)
             mma_ss(d, sdesc_sw128(xa + kk * 32, 16, 1024), sdesc_sw128(wb + kk * 32, 16, 1024), IDESC,
                    (c > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(EMPTY + st));
+          mma_commit_mc(bar(EMPTY + st), (uint16_t)3);  // the stage of both CTAs
           any = true;
         }
         if (ok) mma_commit(bar(TFULL + acc));
@@ -162,9 +189,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
     const int esz = a.out_f32 ? 4 : 2;
     uint32_t i = 0;
-    for (int t = blockIdx.x; t < a.tiles; t += gridDim.x, ++i) {
+    for (int t = cl; t < a.tiles; t += ncl, ++i) {
       const uint32_t acc = i & 1u;
-      const int n0 = (t / a.m_tiles) * TN, m0 = (t % a.m_tiles) * TM;
+      const int n0 = tile_n0(t), m0 = tile_m0(t);
       bool waited = true;
       if (lane == 0)
         waited = mbar_wait_sleepy(bar(TFULL + acc), (i >> 1) & 1, abort_flag, a.dev_status, WAIT_NS,
@@ -256,6 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  cluster_sync_all();  // neither CTA leaves while the peer may still write to it
 }
 
 // [rows][cols] bf16, row stride `ld` elements, boxes of `box_rows` x 64 with
@@ -296,8 +324,8 @@ cudaError_t tc_tgemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s) {
   const int M = g.M, N = g.N, K = g.K;
   Args a;
   a.M = M; a.N = N; a.K = K;
-  a.m_tiles = (M + TM - 1) / TM;
-  a.tiles = a.m_tiles * ((N + TN - 1) / TN);
+  a.m_pairs = ((M + TM - 1) / TM + 1) / 2;
+  a.tiles = a.m_pairs * ((N + TN - 1) / TN);
   a.epi = g.epi;
   a.out = g.out; a.ldo = g.o_ms; a.out_f32 = g.o_f32;
   a.rope = g.rope; a.max_pos = g.max_pos; a.d_r = g.d_r; a.rope_off = g.rope_off;
@@ -315,7 +343,7 @@ cudaError_t tc_tgemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s) {
   CUtensorMap tm_x, tm_w;
   cudaError_t e = make_map(&tm_x, g.a, (uint64_t)M, (uint64_t)K, (uint64_t)ldx, TM);
   if (e != cudaSuccess) return e;
-  e = make_map(&tm_w, g.w, (uint64_t)N, (uint64_t)K, (uint64_t)g.w_ns, TN);
+  e = make_map(&tm_w, g.w, (uint64_t)N, (uint64_t)K, (uint64_t)g.w_ns, TN / 2);
   if (e != cudaSuccess) return e;
   static unsigned long long smem_done = 0;
   e = set_max_smem_once((const void*)tgemm_kernel, (int)SMEM, smem_done);
@@ -323,8 +351,23 @@ cudaError_t tc_tgemm_launch(const GemmArgs& g, long long ldx, cudaStream_t s) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = a.tiles < sms ? a.tiles : sms;
-  tgemm_kernel<<<grid, THREADS, SMEM, s>>>(tm_x, tm_w, a);
+  // clusters of two that can be resident at once (one CTA per SM)
+  static int resident[64];
+  int* res = dev >= 0 && dev < 64 ? &resident[dev] : nullptr;
+  int fit = res && *res > 0 ? *res : 0;
+  if (fit == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)sms);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM;
+    if (cudaOccupancyMaxActiveClusters(&fit, tgemm_kernel, &cfg) != cudaSuccess || fit <= 0) {
+      cudaGetLastError();
+      fit = sms / 2;
+    }
+    if (res) *res = fit;
+  }
+  const int clusters = a.tiles < fit ? a.tiles : fit;
+  tgemm_kernel<<<2 * clusters, THREADS, SMEM, s>>>(tm_x, tm_w, a);
   return cudaGetLastError();
 }
 
