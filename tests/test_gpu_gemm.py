@@ -39,6 +39,7 @@ OUT_PROJ_SHAPES = [
     (1024, 16, 128, 768),   # 8 x 3 tiles, K = 2048
     (2048, 8, 64, 4096),    # 256 tiles: each SM takes two, both accumulators in turn
     (383, 3, 64, 520),      # ragged last token and feature tiles, K = 192
+    (300, 2, 64, 97),       # fp32 rows of 97 features: not in 16-byte pieces
 ]
 
 
@@ -126,6 +127,40 @@ def test_append_many_tokens_across_token_tiles():
     rows = st.cache.double().cpu().numpy()
     got = np.stack([rows[st.bt_np[0, p // 64], p % 64] for p in pos])
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * np.abs(ref).max())
+
+
+def test_append_bad_positions_many_tokens():
+    """300 tokens appended through the tile GEMM with two positions outside
+    the block table (negative, and past it): both are reported as
+    MLA_DEV_BAD_POS and skipped, every other row is written as the oracle
+    says, and no other cache slot changes."""
+    wl = synth.WORKLOADS["tiny_f32_ctx256"].replace(
+        name="prefill_bf16_bad", dtype="bf16", n_h=128, d_h=128, d_r=64, d_c=512, d_v=128,
+        d_model=512, d_cq=0, page_size=64, ctx=300)
+    st = DecodeStep(wl)
+    bad = {5: -1, 200: st.max_pages * wl.page_size + 7}
+    for t, v in bad.items():
+        st.append_pos[t] = v
+    before = st.cache.clone()
+    st.append()
+    torch.cuda.synchronize()
+    assert st.status() & M.MLA_DEV_BAD_POS
+    ex = Expected(wl)
+    pos, c, k = ex.appended_rows(0)
+    ref = np.concatenate([c, k], axis=1)
+    after = st.cache
+    changed = (before.view(torch.int16) != after.view(torch.int16)).any(dim=-1).cpu().numpy()
+    expect = np.zeros_like(changed)
+    rows = after.double().cpu().numpy()
+    for i, p in enumerate(pos):
+        if i in bad:
+            continue
+        blk, r = st.bt_np[0, p // 64], p % 64
+        expect[blk, r] = True
+        got = rows[blk, r]
+        assert np.all(np.abs(got - ref[i]) <= 2.0 ** -8 * np.abs(ref[i]) + 1e-5 * np.abs(ref).max()), i
+    # rows that the oracle writes as exact zeros may leave a slot unchanged
+    assert not np.any(changed & ~expect)
 
 
 def test_layer_step_tensor_core_matches_cuda_core():
