@@ -4,9 +4,11 @@
 A step is one pass of the decode path over one batch of synthetic input
 (default workload: DeepSeek-V2 shapes, batch 32, 4096-token contexts, bf16
 paged cache): absorb_q -> plan -> decode_attn -> combine -> absorb_out, all
-through the C ABI. ``--workload`` picks another of the five workloads; the
-line also carries ``other_workloads``: the long-context, ragged and
-full-layer workloads measured the same way, each with its own roofline.
+through the C ABI. ``--workload`` picks another workload (the FP8 cache
+workload with the suffix ``_staged`` goes through mla_decode_attn_fp8_staged);
+the line also carries ``other_workloads``: the long-context, ragged,
+full-layer, multi-token, prefill and FP8 workloads measured the same way,
+each with its own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -437,7 +439,11 @@ def main():
     mbuild.build()
     from mla_latent_kv_67_b300 import synth
 
-    wl = synth.WORKLOADS.get(args.workload) or synth.EXTRA_WORKLOADS[args.workload]
+    staged = args.workload.endswith(STAGED)  # an FP8 workload through the widening entry
+    base = args.workload[:-len(STAGED)] if staged else args.workload
+    wl = synth.WORKLOADS.get(base) or synth.EXTRA_WORKLOADS[base]
+    if staged:
+        wl = wl.replace(name=args.workload)
     if args.ctx:
         wl = wl.replace(name=f"{wl.name}_ctx{args.ctx}", ctx=args.ctx, ctx_range=None, lens=None)
     stream = torch.cuda.current_stream()
@@ -456,7 +462,7 @@ def main():
     K = args.steps
     sampler = ClockSampler(local)
     st, graph, res = measure_workload(wl, dev, K, args.warmup, flush, stream, hbm, tflops,
-                                      barrier=barrier, sampler=sampler)
+                                      barrier=barrier, sampler=sampler, fp8_staged=staged)
     stages = st.stages()
 
     # the same step, call by call (eager), for comparison
