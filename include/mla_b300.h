@@ -353,7 +353,8 @@ mla_status mla_decode_attn_static(const void* q_cat, const void* cache,
  *              bf16 plan and partials, the identity table and
  *              B * max_pages * page_size * (d_c + d_r) bf16 rows.
  * Errors: as mla_decode_attn; MLA_ERR_UNSUPPORTED for B > 65535 or d_r not
- * a multiple of 8. Block ids outside [0, num_pages) are reported through
+ * a multiple of 8; MLA_ERR_INVALID_ARG for a cache not 16-byte aligned or a
+ * workspace not 256-byte aligned. Block ids outside [0, num_pages) are reported through
  * dev_status (MLA_DEV_BAD_BLOCK) and read as zero rows. The workspace size
  * depends on the decode kernel the device selects; query it under the same
  * mla_force_decode_path setting as the call. */

@@ -65,6 +65,15 @@ def test_host_validation_rejects_bad_arguments():
     st = lib.mla_decode_attn(None, None, None, 1, 1, None, -1, 1.0, None, 0, None, None,
                              M.MLA_BF16, ctypes.byref(d), None, None)
     assert st == M.MLA_ERR_INVALID_ARG
+    # the FP8 staged decode: negative batch, NULL tensors
+    st = lib.mla_decode_attn_fp8_staged(None, None, None, 1, 1, None, -1, 1.0, None, 0, None, None,
+                                        ctypes.byref(d), None, None)
+    assert st == M.MLA_ERR_INVALID_ARG
+    st = lib.mla_decode_attn_fp8_staged(None, None, None, 1, 1, None, 2, 1.0, None, 0, None, None,
+                                        ctypes.byref(d), None, None)
+    assert st == M.MLA_ERR_INVALID_ARG and b"NULL" in lib.mla_last_error()
+    assert lib.mla_decode_fp8_staged_workspace_size(0, 4, ctypes.byref(d)) == 0
+    assert lib.mla_decode_fp8_staged_workspace_size(2, 0, ctypes.byref(d)) == 0
     # append without d_model
     st = lib.mla_append_latent(1, 1, None, 1, 1, 1, 1, 1, 1, 1, 1, 1, M.MLA_BF16,
                                ctypes.byref(d), None, None)
@@ -76,6 +85,8 @@ def test_empty_batch_is_a_no_op():
     d = _dims()
     assert lib.mla_absorb_q(None, None, None, 0, M.MLA_BF16, ctypes.byref(d), None) == M.MLA_OK
     assert lib.mla_combine(None, 0, 0, None, None, M.MLA_BF16, ctypes.byref(d), None) == M.MLA_OK
+    assert lib.mla_decode_attn_fp8_staged(None, None, None, 1, 1, None, 0, 1.0, None, 0, None, None,
+                                          ctypes.byref(d), None, None) == M.MLA_OK
 
 
 def test_binding_refuses_cpu_tensors():
