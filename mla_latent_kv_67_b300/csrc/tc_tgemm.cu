@@ -224,6 +224,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll 1
       for (int b = 0; b < TN / 32; ++b) {
         uint32_t v[32];
+        __syncwarp();  // rows past M skip the stores below: converge for the warp-wide load
         tmem_ld32(tmem + lane_addr + acc * TN + b * 32, v);
         tmem_ld_wait();
         if (b == TN / 32 - 1) {  // the accumulator is read out: hand it back
